@@ -1,0 +1,546 @@
+#!/usr/bin/env python
+"""Benchmark of the attention-prologue hot path on GB300 (one JSON line).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. fused_qk_norm_rope on packed bf16 QKV [32768, (32+8+8)*128], theta 1e6,
+     positions uniform in [0, 131072) -- Q and K normalised and rotated in
+     place, V untouched;
+  2. dsv4_qnorm_rope_kv_rope_quant_insert on q bf16 [32768, 64, 512] and kv
+     [32768, 512], positions uniform in [0, 131072), 65536-slot paged cache,
+     slot_mapping a random permutation prefix.
+The metric is achieved HBM bandwidth: algorithmic bytes of the step (every
+byte the operators must read or write once) / device time of the step, in
+GB/s.  Inputs are resident in HBM and larger than L2 (129 MB), so no L2 flush
+is needed between steps.
+
+--impl reference times the CPU oracle (the only other implementation of this
+path available here) on a bounded sample of the same workload.
+--sweep additionally writes per-configuration lines (every workload of the
+parity tests, both launch shapes, the dispatch crossover and a 512 MiB
+device-to-device copy ceiling) to stderr.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "achieved HBM GB/s and % of GB300 peak, fused norm+RoPE(+quant+insert)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def qk_bytes(T, Hq, Hk, D=128):
+    """Q and K heads read and written once (bf16), one cos/sin row (fp32) and
+    one position (int64) per token, the two weight vectors once."""
+    return T * ((Hq + Hk) * D * 2 * 2 + D * 4 + 8) + 2 * D * 2
+
+
+def dsv4_bytes(T, H, mapped):
+    """q read + written (bf16), kv read (bf16), one 64-float cos/sin row,
+    position and slot (int64) per token; 584 bytes per mapped token written;
+    the two weight vectors once."""
+    return T * (H * 512 * 2 * 2 + 512 * 2 + 64 * 4 + 8 + 8) + mapped * 584 + 2 * 512 * 2
+
+
+def step_bytes(qk, ds):
+    return (qk_bytes(qk["qkv"].shape[0], qk["Hq"], qk["Hk"], qk["D"]),
+            dsv4_bytes(ds["q"].shape[0], ds["H"], int((ds["slot_mapping"] >= 0).sum())))
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_quant_cache_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_tag):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (profiles/*.md carry 'source-hash: <h>' and
+    'traffic-bytes-per-launch: <n>' lines)."""
+    want = kernel_source_hash()
+    if not os.path.isdir(PROFILES):
+        return None
+    for f in sorted(os.listdir(PROFILES)):
+        if not f.startswith(kernel_tag):
+            continue
+        text = open(os.path.join(PROFILES, f)).read()
+        m_h = re.search(r"source-hash:\s*([0-9a-f]+)", text)
+        m_t = re.search(r"traffic-bytes-per-launch:\s*([0-9.eE+]+)", text)
+        if m_h and m_t and m_h.group(1) == want:
+            return float(m_t.group(1))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data exchange)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def make_step_inputs(device):
+    qk = wl.make_qk_workload(wl.QK_LARGE, device=device)
+    ds = wl.make_dsv4_workload(wl.DSV4_LARGE, device=device)
+    return qk, ds
+
+
+def launch_qk(kvq, qk, stream):
+    kvq.fused_qk_norm_rope(qk["qkv"], qk["Hq"], qk["Hk"], qk["Hv"], qk["D"], qk["eps"],
+                           qk["q_weight"], qk["k_weight"], qk["cos_sin"], True, qk["positions"],
+                           stream=stream)
+
+
+def launch_dsv4(kvq, ds, stream):
+    kvq.dsv4_qnorm_rope_kv_rope_quant_insert(ds["q"], ds["kv"], ds["eps"], ds["q_weight"],
+                                             ds["kv_weight"], ds["cos_sin"], ds["positions"],
+                                             ds["slot_mapping"], ds["kv_cache"], stream=stream)
+
+
+def time_device(kvq, qk, ds, steps, warmup, world, device):
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch_qk(kvq, qk, stream)
+            launch_dsv4(kvq, ds, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for e0, e1, e2 in ev:
+            e0.record(stream)
+            launch_qk(kvq, qk, stream)
+            e1.record(stream)
+            launch_dsv4(kvq, ds, stream)
+            e2.record(stream)
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    qk_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    ds_ms = [b.elapsed_time(c) for _, b, c in ev]
+    return total_ms, qk_ms, ds_ms
+
+
+def time_e2e(kvq, qk, ds, steps, device):
+    """Same step with host buffers: pinned inputs copied in, the kernels, the
+    results (q, qkv, cache) copied out, every step inside the timed region."""
+    h = {
+        "qkv": qk["qkv"].cpu().pin_memory(), "qk_pos": qk["positions"].cpu().pin_memory(),
+        "q": ds["q"].cpu().pin_memory(), "kv": ds["kv"].cpu().pin_memory(),
+        "ds_pos": ds["positions"].cpu().pin_memory(), "slot": ds["slot_mapping"].cpu().pin_memory(),
+    }
+    out = {"qkv": torch.empty_like(h["qkv"]).pin_memory(), "q": torch.empty_like(h["q"]).pin_memory(),
+           "cache": torch.empty(ds["kv_cache"].shape, dtype=torch.uint8).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for t in out.values())
+    stream = torch.cuda.Stream(device)
+
+    def one():
+        qk["qkv"].copy_(h["qkv"], non_blocking=True)
+        qk["positions"].copy_(h["qk_pos"], non_blocking=True)
+        ds["q"].copy_(h["q"], non_blocking=True)
+        ds["kv"].copy_(h["kv"], non_blocking=True)
+        ds["positions"].copy_(h["ds_pos"], non_blocking=True)
+        ds["slot_mapping"].copy_(h["slot"], non_blocking=True)
+        launch_qk(kvq, qk, stream)
+        launch_dsv4(kvq, ds, stream)
+        out["qkv"].copy_(qk["qkv"], non_blocking=True)
+        out["q"].copy_(ds["q"], non_blocking=True)
+        out["cache"].copy_(ds["kv_cache"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+        stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            one()
+        end.record(stream)
+    stream.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_baseline(sample_tokens=4096):
+    """The oracle as it stands, all host cores, on the first `sample_tokens`
+    tokens of both workloads of the step (inputs generated on the CPU with the
+    same recipe).  Returns (GB/s by the same byte count, threads, description)."""
+    import oracle
+    qk = wl.make_qk(sample_tokens, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001)
+    ds = wl.make_dsv4(sample_tokens, 64, max_pos=131072, num_blocks=1024, block_size=64,
+                      slots="perm_prefix", seed=1003)
+    qk_in = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
+             for k, v in qk.items() if isinstance(v, torch.Tensor)}
+    ds_in = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
+             for k, v in ds.items() if isinstance(v, torch.Tensor)}
+    cache = ds_in["kv_cache"].copy()
+    t0 = time.perf_counter()
+    oracle.qk_norm_rope(qk_in["qkv"], 32, 8, 8, 128, qk["eps"], qk_in["q_weight"],
+                        qk_in["k_weight"], qk_in["cos_sin"], qk_in["positions"])
+    oracle.dsv4(ds_in["q"], ds_in["kv"], ds["eps"], ds_in["q_weight"], ds_in["kv_weight"],
+                ds_in["cos_sin"], ds_in["positions"], ds_in["slot_mapping"], cache)
+    dt = time.perf_counter() - t0
+    nbytes = qk_bytes(sample_tokens, 32, 8) + dsv4_bytes(sample_tokens, 64, sample_tokens)
+    return nbytes / dt / 1e9, oracle.default_threads(), dt, (
+        f"first {sample_tokens} of 32768 tokens of both operators of the step (fp64 oracle)")
+
+
+def config_block(extra=None):
+    c = {"workload": "fused_qk_norm_rope T=32768 Hq/Hk/Hv=32/8/8 D=128 theta=1e6 + "
+                     "dsv4_qnorm_rope_kv_rope_quant_insert T=32768 H=64 (65536-slot cache)",
+         "tokens_per_step": 32768, "qk_heads": [32, 8, 8], "dsv4_heads": 64,
+         "l2": "inputs larger than L2 (qkv 403 MB, q 2.1 GB); no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_gpu(args):
+    import kv_quant_cache_gb300 as kvq
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    kvq.lib()
+    qk, ds = make_step_inputs(device)
+    b_qk, b_ds = step_bytes(qk, ds)
+    warmup = max(args.warmup, 3)
+    clocks = ClockSampler(local)
+    total_ms, qk_ms, ds_ms = time_device(kvq, qk, ds, args.steps, warmup, world, device)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(total_ms, world, device)
+    ms_step = total_ms / args.steps
+    value = world * (b_qk + b_ds) / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = peak_hbm()
+    ds_avg = statistics.mean(ds_ms)
+    qk_avg = statistics.mean(qk_ms)
+    achieved = b_ds / (ds_avg * 1e-3) / 1e9
+    traffic = recorded_traffic("dsv4_tiled_T32768_H64")
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        e2e_ms, h2d, d2h = time_e2e(kvq, qk, ds, e2e_steps, device)
+        e2e_ms = max_over_ranks(e2e_ms, world, device)
+        e2e = {"value": round(world * (b_qk + b_ds) / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+               "steps": e2e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, dt, sample = cpu_baseline(args.cpu_sample_tokens)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample, "seconds": round(dt, 2)}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_block({
+            "algorithmic_bytes_per_step": b_qk + b_ds, "qk_bytes": b_qk, "dsv4_bytes": b_ds,
+            "qk_ms": round(qk_avg, 5), "dsv4_ms": round(ds_avg, 5),
+            "qk_gbs": round(b_qk / (qk_avg * 1e-3) / 1e9, 1),
+            "pct_of_peak": round(100 * value / world / peak, 2),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": {"bound": "hbm", "kernel": "dsv4_kernel<8,4,1> (token-tiled)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": b_ds},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if args.sweep and rank == 0:
+        sweep(kvq, device)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    S = args.cpu_sample_tokens
+    qk = wl.make_qk(S, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001)
+    ds = wl.make_dsv4(S, 64, max_pos=131072, num_blocks=1024, block_size=64,
+                      slots="perm_prefix", seed=1003)
+    qkv = wl.bf16_bits(qk["qkv"])
+    qq = wl.bf16_bits(ds["q"])
+    host = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
+            for k, v in {**{"qw": qk["q_weight"], "kw": qk["k_weight"], "cs1": qk["cos_sin"],
+                            "p1": qk["positions"]},
+                         **{"dqw": ds["q_weight"], "dkw": ds["kv_weight"], "kv": ds["kv"],
+                            "cs2": ds["cos_sin"], "p2": ds["positions"],
+                            "slot": ds["slot_mapping"], "cache": ds["kv_cache"]}}.items()}
+
+    def step():
+        oracle.qk_norm_rope(qkv, 32, 8, 8, 128, qk["eps"], host["qw"], host["kw"], host["cs1"],
+                            host["p1"], out=qkv)
+        oracle.dsv4(qq, host["kv"], ds["eps"], host["dqw"], host["dkw"], host["cs2"], host["p2"],
+                    host["slot"], host["cache"], q_out=qq)
+
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = qk_bytes(S, 32, 8) + dsv4_bytes(S, 64, S)
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block({"sample_tokens_per_step": S}),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle",
+                         "cores": oracle.default_threads(),
+                         "sample": f"first {S} of 32768 tokens of both operators per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# sweep: every parity workload, both launch shapes, copy ceiling
+# ---------------------------------------------------------------------------
+
+def _time_launch(fn, reps, stream, flush=None):
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.add_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(x.elapsed_time(y) for x, y in times)
+    return ms[len(ms) // 2], ms[0]
+
+
+def sweep(kvq, device):
+    peak, _ = peak_hbm()
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
+    out = []
+    # device-to-device copy ceiling (counting read + write)
+    src = torch.empty(512 * 2**20, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    med, best = _time_launch(lambda: dst.copy_(src), 20, stream)
+    out.append({"sweep": "d2d_copy_512MiB", "gbs_median": round(2 * src.numel() / med / 1e6, 1),
+                "gbs_best": round(2 * src.numel() / best / 1e6, 1)})
+    del src, dst
+    for w in (wl.QK_SMALL, wl.QK_LARGE):
+        d = wl.make_qk_workload(w, device=device)
+        nb = qk_bytes(w.T, w.Hq, w.Hk)
+        small = nb < 256 * 2**20
+        med, best = _time_launch(lambda: launch_qk(kvq, d, stream), 50, stream,
+                                 flush if small else None)
+        out.append({"sweep": w.name, "bytes": nb, "us_median": round(med * 1e3, 2),
+                    "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
+                    "l2_flush": small})
+        del d
+    ds_work = [wl.DSV4_DECODE, wl.DSV4_LARGE, *wl.DSV4_SWEEP]
+    for w in ds_work:
+        d = wl.make_dsv4_workload(w, device=device)
+        mapped = int((d["slot_mapping"] >= 0).sum())
+        nb = dsv4_bytes(w.T, w.H, mapped)
+        small = nb < 256 * 2**20
+        for path, thr in (("auto", -1), ("small", 1 << 40), ("tiled", 0)):
+            old = kvq.set_dsv4_dispatch_threshold(thr)
+            try:
+                med, best = _time_launch(lambda: launch_dsv4(kvq, d, stream),
+                                         50 if nb < 2**30 else 15, stream, flush if small else None)
+            finally:
+                kvq.set_dsv4_dispatch_threshold(old)
+            out.append({"sweep": w.name, "path": path, "bytes": nb, "us_median": round(med * 1e3, 2),
+                        "gbs": round(nb / med / 1e6, 1),
+                        "pct_peak": round(100 * nb / med / 1e6 / peak, 1), "l2_flush": small})
+        del d
+    # dispatch crossover: program count T * (H + 1) at which tiled starts to win
+    for H in (64, 128):
+        for T in (1, 2, 4, 8, 16, 32, 64, 128, 192, 256, 384, 512, 1024):
+            d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 64), block_size=64,
+                             seed=7 + T, device=device)
+            res = {}
+            for path, thr in (("small", 1 << 40), ("tiled", 0)):
+                old = kvq.set_dsv4_dispatch_threshold(thr)
+                try:
+                    res[path] = _time_launch(lambda: launch_dsv4(kvq, d, stream), 50, stream, flush)[0]
+                finally:
+                    kvq.set_dsv4_dispatch_threshold(old)
+            out.append({"sweep": "dispatch", "T": T, "H": H, "programs": T * (H + 1),
+                        "small_us": round(res["small"] * 1e3, 2), "tiled_us": round(res["tiled"] * 1e3, 2)})
+            del d
+    for o in out:
+        sys.stderr.write(json.dumps(o) + "\n")
+    sys.stderr.flush()
+
+
+def run_profile_case(args):
+    """A reduced case of one kernel for profiler captures: --profile qk|dsv4,
+    --tokens T, --heads H, --launches n (each launch on the same inputs)."""
+    import kv_quant_cache_gb300 as kvq
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(device)
+    if args.profile == "qk":
+        d = wl.make_qk(args.tokens, args.heads, 8, 8, theta=1e6, max_pos=131072, seed=1001,
+                       device=device)
+        fn, nb = (lambda: launch_qk(kvq, d, stream)), qk_bytes(args.tokens, args.heads, 8)
+    else:
+        d = wl.make_dsv4(args.tokens, args.heads, max_pos=131072,
+                         num_blocks=-(-2 * args.tokens // 64), block_size=64, seed=1003,
+                         device=device)
+        fn, nb = (lambda: launch_dsv4(kvq, d, stream)), dsv4_bytes(args.tokens, args.heads, args.tokens)
+    med, best = _time_launch(fn, args.launches, stream)
+    print(json.dumps({"profile": args.profile, "tokens": args.tokens, "heads": args.heads,
+                      "bytes": nb, "us_median": round(med * 1e3, 2),
+                      "gbs": round(nb / med / 1e6, 1)}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("kvq", "reference"), default="kvq")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--profile", choices=("qk", "dsv4"), default=None)
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--heads", type=int, default=64)
+    ap.add_argument("--launches", type=int, default=5)
+    args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

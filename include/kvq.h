@@ -1,0 +1,171 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) attention-prologue kernels.
+ *
+ * Two operators of the memory-bound per-token prologue that runs between the
+ * QKV projection and attention in LLM serving:
+ *
+ *   fused_qk_norm_rope
+ *       per-head RMSNorm + NeoX rotary embedding, in place, on the Q and K
+ *       heads of a packed bf16 QKV tensor; V is neither read nor written.
+ *       Source: InfiniOps PR #1019, "Add the NineToothed NVIDIA implementation
+ *       of FusedQkNormRope", sections "Summary" (semantics, parameter order
+ *       aligned with vLLM's fused_qk_norm_rope, separate [D] weights, the
+ *       paired dimension's weight applied to the NeoX partner) and "Notes for
+ *       Reviewers" (the guarded fast path: bf16, head_dim 128, full-dimension
+ *       NeoX rotation, contiguous packed QKV, contiguous int64 positions).
+ *
+ *   dsv4_qnorm_rope_kv_rope_quant_insert
+ *       DeepSeek-V4-style prologue: per-head RMSNorm + RoPE of q in place, and
+ *       RMSNorm + RoPE of the one shared KV vector per token, whose non-rotary
+ *       part is quantised to FP8 e4m3 with one UE8M0 (power-of-two) scale per
+ *       64-element block and written, with its rotary part, into a paged cache
+ *       through slot_mapping.
+ *       Sources: FlagGems PR #5449, "[KMCompiler][Hygon] Token-tiled
+ *       fused_deepseek_v4_qnorm_rope_kv_rope_quant_insert", section
+ *       "Performance" (the operator takes slot_mapping and kv_cache and carries
+ *       seven per-block exponents per token), and FlagGems PR #5321,
+ *       "[KMCompiler][MetaX][Hygon] Token-tiled ... plus test and benchmark
+ *       fixes", section "What the optimisation does" (H query-head slots plus
+ *       one KV slot per token; the KV slot does seven quantisation blocks).
+ *       The pages fix neither the split of the 512-wide slot nor the cache
+ *       entry; this library defines them as listed below.
+ *
+ * General contract (both operators)
+ *   - All pointers are DEVICE pointers of the current CUDA device and are
+ *     owned by the caller.  The library allocates no memory, keeps no
+ *     per-call state, and never synchronises the stream.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream).  A KVQ_OK
+ *     return means "validated and enqueued"; kernel faults surface on the
+ *     stream like any other kernel's.
+ *   - Arguments are validated on the host before anything is launched.  On
+ *     any error status nothing was launched and no memory was touched.
+ *   - num_tokens == 0 returns KVQ_OK without a launch (pointers may be NULL).
+ *   - After the launch the CUDA launch error (if any) is fetched and cleared
+ *     with cudaGetLastError and reported as KVQ_ERR_CUDA; the raw code is
+ *     available from kvq_last_cuda_error().
+ *   - Not checked (no sizes cross the ABI for them; the caller guarantees):
+ *     0 <= positions[t] < rows of cos_sin_cache; slot_mapping[t] == -1 or a
+ *     slot inside the cache; no two tokens map to the same slot; q/qkv do not
+ *     overlap the cache.  Violations are undefined behaviour.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Layout-compatible with cudaStream_t of the CUDA runtime. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_NULL = 1,        /* a required pointer is NULL */
+  KVQ_ERR_SHAPE = 2,       /* negative or too-large count, bad block_size */
+  KVQ_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
+  KVQ_ERR_ALIGN = 4,       /* a pointer is not aligned as required below */
+  KVQ_ERR_CUDA = 5,        /* the kernel launch itself failed */
+  KVQ_ERR_VALUE = 6        /* eps negative or not finite */
+} kvq_status;
+
+/*
+ * fused_qk_norm_rope -- in place on qkv.
+ *
+ *   qkv            bf16 [num_tokens, (Hq + Hk + Hv) * head_dim], row-major,
+ *                  contiguous, 16-byte aligned.  Per token: Hq query heads,
+ *                  then Hk key heads, then Hv value heads, head_dim each.
+ *                  Q and K heads are replaced by their normalised, rotated
+ *                  values; V heads are not accessed.
+ *   num_tokens     T >= 0 (T * (Hq + Hk) must stay below 2^31).
+ *   num_heads_q/k/v  >= 0 each.
+ *   head_dim       must be 128 (else KVQ_ERR_UNSUPPORTED).
+ *   eps            added to the mean square inside the square root; finite,
+ *                  >= 0.
+ *   q_weight, k_weight  bf16 [head_dim] RMSNorm weights, 16-byte aligned.
+ *   cos_sin_cache  fp32 [max_pos, head_dim]; row p holds cos(p * f_i) for
+ *                  i < head_dim/2 followed by sin(p * f_i); 16-byte aligned.
+ *   is_neox        must be 1: dim i pairs with dim i + head_dim/2 (else
+ *                  KVQ_ERR_UNSUPPORTED).
+ *   positions      int64 [num_tokens], 8-byte aligned, each < max_pos.
+ *
+ * Per head row x (fp32 arithmetic, one bf16 round-to-nearest-even at the end):
+ *   r = 1 / sqrt(sum(x^2) / head_dim + eps);  n_i = x_i * r * w_i
+ *   out_i       = n_i * cos_i - n_{i+64} * sin_i        (i < 64)
+ *   out_{i+64}  = n_{i+64} * cos_i + n_i * sin_i
+ * so the partner enters with its own dimension's weight.
+ */
+kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
+                              int num_heads_k, int num_heads_v, int head_dim,
+                              float eps, const void* q_weight,
+                              const void* k_weight, const float* cos_sin_cache,
+                              int is_neox, const int64_t* positions,
+                              kvq_stream_t stream);
+
+/*
+ * dsv4_qnorm_rope_kv_rope_quant_insert -- q in place, cache entries written.
+ *
+ *   q              bf16 [num_tokens, num_heads, 512], contiguous, 16-byte
+ *                  aligned; every head row is normalised with q_weight and
+ *                  its last 64 dims rotated, in place, whether or not the
+ *                  token has a cache slot.
+ *   kv             bf16 [num_tokens, 512], contiguous, 16-byte aligned; read
+ *                  only.
+ *   num_tokens     T >= 0; num_heads H >= 1 (T * (H + 1) below 2^31).
+ *   eps            finite, >= 0.
+ *   q_weight, kv_weight  bf16 [512], 16-byte aligned.
+ *   cos_sin_cache  fp32 [max_pos, 64]: 32 cosines then 32 sines per row;
+ *                  16-byte aligned.
+ *   positions      int64 [num_tokens], 8-byte aligned.
+ *   slot_mapping   int64 [num_tokens], 8-byte aligned; -1 = no cache write.
+ *   kv_cache       uint8 [num_blocks, block_size, 584], contiguous, 8-byte
+ *                  aligned; slot s is the 584 bytes at offset s * 584.
+ *   block_size     >= 1 (the cache's second dimension).
+ *
+ * RoPE (both q and kv): interleaved pairs (448 + 2i, 449 + 2i), i < 32, with
+ * cos/sin column i of row positions[t].
+ * Cache entry of a token with slot s >= 0 (n = normalised, rotated kv, fp32):
+ *   bytes [0, 448)    e4m3fn codes of n_j * 2^-e_b, round to nearest even,
+ *                     j = 64 b + k for blocks b = 0..6
+ *   bytes [448, 576)  n_448 .. n_511 as bf16, little endian
+ *   bytes [576, 583)  UE8M0 exponent bytes e_b + 127, b = 0..6, where e_b is
+ *                     the smallest integer with 448 * 2^e_b >= max_k |n_64b+k|,
+ *                     clamped to [0, 254]
+ *   byte  583         0
+ * Other cache bytes are never written.
+ *
+ * Launch shape: a program count T * (H + 1) below the dispatch threshold
+ * (kvq_dsv4_dispatch_threshold) takes the small-batch launch, otherwise the
+ * token-tiled one.  Results do not depend on the choice.
+ */
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
+    void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int block_size, kvq_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* kvq_status_string(kvq_status status);
+
+/* The cudaError_t value behind the most recent KVQ_ERR_CUDA returned on the
+ * calling thread (0 if none). */
+int kvq_last_cuda_error(void);
+
+/* Program-count threshold of the DSV4 launch-shape dispatch.  The default is
+ * the crossover measured on GB300; the environment variable
+ * KVQ_DSV4_DISPATCH_THRESHOLD, read once at the first call that needs it,
+ * overrides it (0 = always the token-tiled launch). */
+int64_t kvq_dsv4_dispatch_threshold(void);
+/* Set the threshold (value >= 0) or restore the default/environment value
+ * (value < 0).  Returns the previous threshold.  Not synchronised with
+ * concurrent launches on other threads. */
+int64_t kvq_set_dsv4_dispatch_threshold(int64_t value);
+/* Which launch a call with these sizes takes: 0 small-batch, 1 token-tiled. */
+int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

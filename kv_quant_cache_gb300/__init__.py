@@ -1,0 +1,159 @@
+"""GB300 (sm_103a) attention-prologue kernels -- Python binding of include/kvq.h.
+
+This module only marshals arguments: it checks that tensors are CUDA tensors of
+the expected dtype and layout, takes their device pointers and the current
+stream, and calls the C ABI in ``libkvq.so``.  Every step of the computation
+runs in the CUDA kernels; there is no CPU or PyTorch fallback.  If the library
+has not been built, importing works but every call raises ``KvqError``.
+
+Build: ``python -m kv_quant_cache_gb300._build`` (or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libkvq.so")
+
+KVQ_OK = 0
+KVQ_ERR_NULL = 1
+KVQ_ERR_SHAPE = 2
+KVQ_ERR_UNSUPPORTED = 3
+KVQ_ERR_ALIGN = 4
+KVQ_ERR_CUDA = 5
+KVQ_ERR_VALUE = 6
+
+ENTRY_BYTES = 584
+DSV4_DIM = 512
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(what)
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    L.fused_qk_norm_rope.restype = _I
+    L.fused_qk_norm_rope.argtypes = [_P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P]
+    L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = _I
+    L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [_P, _P, _I64, _I, _F, _P, _P, _P, _P,
+                                                       _P, _P, _I, _P]
+    L.kvq_status_string.restype = ctypes.c_char_p
+    L.kvq_status_string.argtypes = [_I]
+    L.kvq_last_cuda_error.restype = _I
+    L.kvq_last_cuda_error.argtypes = []
+    L.kvq_dsv4_dispatch_threshold.restype = _I64
+    L.kvq_dsv4_dispatch_threshold.argtypes = []
+    L.kvq_set_dsv4_dispatch_threshold.restype = _I64
+    L.kvq_set_dsv4_dispatch_threshold.argtypes = [_I64]
+    L.kvq_dsv4_dispatch_path.restype = _I
+    L.kvq_dsv4_dispatch_path.argtypes = [_I64, _I]
+    return L
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises KvqError if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise KvqError(-1, f"{LIB_PATH} not found: build it with "
+                               "`python -m kv_quant_cache_gb300._build`")
+        _LIB = _declare(ctypes.CDLL(LIB_PATH))
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+def _check(status: int, fn: str) -> None:
+    if status != KVQ_OK:
+        msg = f"{fn}: {status_string(status)}"
+        if status == KVQ_ERR_CUDA:
+            msg += f" (cudaError {lib().kvq_last_cuda_error()})"
+        raise KvqError(status, msg)
+
+
+def _cuda(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
+                       q_weight, k_weight, cos_sin_cache, is_neox, positions,
+                       stream=None) -> None:
+    """In-place per-head RMSNorm + NeoX RoPE of the Q and K heads of ``qkv``.
+
+    qkv: bf16 [T, (Hq+Hk+Hv)*head_dim]; weights bf16 [head_dim]; cos_sin_cache
+    fp32 [max_pos, head_dim]; positions int64 [T].  Same parameter order as
+    the C entry point (stream last, default: torch's current stream).
+    """
+    if qkv.dim() != 2 or qkv.shape[1] != (num_heads_q + num_heads_k + num_heads_v) * head_dim:
+        raise ValueError("qkv must be [T, (Hq+Hk+Hv)*head_dim]")
+    T = qkv.shape[0]
+    st = lib().fused_qk_norm_rope(
+        _cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
+        head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
+        _cuda(k_weight, torch.bfloat16, "k_weight"),
+        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"), int(bool(is_neox)),
+        _cuda(positions, torch.int64, "positions"), _stream(stream, qkv.device))
+    _check(st, "fused_qk_norm_rope")
+
+
+def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_sin_cache,
+                                         positions, slot_mapping, kv_cache,
+                                         stream=None) -> None:
+    """DSV4 prologue: q [T,H,512] normalised + rotated in place; the kv
+    vectors [T,512] normalised, rotated, quantised and written to
+    ``kv_cache`` uint8 [num_blocks, block_size, 584] at ``slot_mapping``."""
+    if q.dim() != 3 or q.shape[2] != DSV4_DIM:
+        raise ValueError("q must be [T, H, 512]")
+    if kv.dim() != 2 or kv.shape[0] != q.shape[0] or kv.shape[1] != DSV4_DIM:
+        raise ValueError("kv must be [T, 512]")
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != ENTRY_BYTES:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 584]")
+    T, H = q.shape[0], q.shape[1]
+    st = lib().dsv4_qnorm_rope_kv_rope_quant_insert(
+        _cuda(q, torch.bfloat16, "q"), _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
+        _cuda(q_weight, torch.bfloat16, "q_weight"), _cuda(kv_weight, torch.bfloat16, "kv_weight"),
+        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"),
+        _cuda(positions, torch.int64, "positions"), _cuda(slot_mapping, torch.int64, "slot_mapping"),
+        _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1], _stream(stream, q.device))
+    _check(st, "dsv4_qnorm_rope_kv_rope_quant_insert")
+
+
+def dsv4_dispatch_threshold() -> int:
+    return lib().kvq_dsv4_dispatch_threshold()
+
+
+def set_dsv4_dispatch_threshold(value: int) -> int:
+    """Set the DSV4 program-count threshold (< 0 restores the default); returns the old one."""
+    return lib().kvq_set_dsv4_dispatch_threshold(int(value))
+
+
+def dsv4_dispatch_path(num_tokens: int, num_heads: int) -> int:
+    return lib().kvq_dsv4_dispatch_path(int(num_tokens), int(num_heads))

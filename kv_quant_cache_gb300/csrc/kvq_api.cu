@@ -1,0 +1,145 @@
+// kvq_api.cu -- the C ABI (include/kvq.h): host-side validation, launch-shape
+// dispatch and launch on the caller's stream.  No allocation, no sync.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+
+#include "kvq.h"
+#include "kvq_launch.h"
+
+namespace {
+
+// Program-count crossover (T * (H + 1)) between the small-batch and the
+// token-tiled DSV4 launch, measured on GB300 by the benchmark's dispatch sweep.
+constexpr int64_t kDefaultDsv4Threshold = 16384;
+
+std::atomic<int64_t> g_threshold{-1};
+std::once_flag g_env_once;
+int64_t g_env_threshold = -1;
+thread_local int t_last_cuda_error = 0;
+
+int64_t env_threshold() {
+  std::call_once(g_env_once, [] {
+    const char* s = std::getenv("KVQ_DSV4_DISPATCH_THRESHOLD");
+    if (s && *s) {
+      char* end = nullptr;
+      const long long v = std::strtoll(s, &end, 10);
+      if (end && *end == '\0' && v >= 0) g_env_threshold = v;
+    }
+  });
+  return g_env_threshold >= 0 ? g_env_threshold : kDefaultDsv4Threshold;
+}
+
+int64_t current_threshold() {
+  const int64_t v = g_threshold.load(std::memory_order_relaxed);
+  return v >= 0 ? v : env_threshold();
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvq_status finish_launch(cudaError_t e) {
+  if (e == cudaSuccess) return KVQ_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return KVQ_ERR_CUDA;
+}
+
+constexpr int64_t kIndexLimit = (int64_t)1 << 31;
+
+}  // namespace
+
+extern "C" {
+
+kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
+                              int num_heads_k, int num_heads_v, int head_dim,
+                              float eps, const void* q_weight,
+                              const void* k_weight, const float* cos_sin_cache,
+                              int is_neox, const int64_t* positions,
+                              kvq_stream_t stream) {
+  if (num_tokens < 0 || num_heads_q < 0 || num_heads_k < 0 || num_heads_v < 0)
+    return KVQ_ERR_SHAPE;
+  if (head_dim != 128 || is_neox != 1) return KVQ_ERR_UNSUPPORTED;
+  if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
+  const int rows = num_heads_q + num_heads_k;
+  if ((int64_t)rows + num_heads_v > (1 << 20) || num_tokens * (int64_t)(rows + 1) >= kIndexLimit)
+    return KVQ_ERR_SHAPE;
+  if (num_tokens == 0 || rows == 0) return KVQ_OK;
+  if (!qkv || !q_weight || !k_weight || !cos_sin_cache || !positions) return KVQ_ERR_NULL;
+  if (!aligned(qkv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) ||
+      !aligned(cos_sin_cache, 16) || !aligned(positions, 8))
+    return KVQ_ERR_ALIGN;
+  kvq::QkArgs a;
+  a.qkv = qkv;
+  a.q_weight = q_weight;
+  a.k_weight = k_weight;
+  a.cos_sin = cos_sin_cache;
+  a.positions = positions;
+  a.num_tokens = (int)num_tokens;
+  a.num_heads_q = num_heads_q;
+  a.num_heads_k = num_heads_k;
+  a.num_heads_v = num_heads_v;
+  a.eps = eps;
+  return finish_launch(kvq::launch_qk_norm_rope(
+      a, kvq::qk_path(num_tokens, rows), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
+    void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int block_size, kvq_stream_t stream) {
+  if (num_tokens < 0 || num_heads < 1 || block_size < 1) return KVQ_ERR_SHAPE;
+  if (num_tokens * (int64_t)(num_heads + 1) >= kIndexLimit) return KVQ_ERR_SHAPE;
+  if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!q || !kv || !q_weight || !kv_weight || !cos_sin_cache || !positions || !slot_mapping ||
+      !kv_cache)
+    return KVQ_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(kv_weight, 16) ||
+      !aligned(cos_sin_cache, 16) || !aligned(positions, 8) || !aligned(slot_mapping, 8) ||
+      !aligned(kv_cache, 8))
+    return KVQ_ERR_ALIGN;
+  kvq::Dsv4Args a;
+  a.q = q;
+  a.kv = kv;
+  a.q_weight = q_weight;
+  a.kv_weight = kv_weight;
+  a.cos_sin = cos_sin_cache;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.kv_cache = kv_cache;
+  a.num_tokens = (int)num_tokens;
+  a.num_heads = num_heads;
+  a.eps = eps;
+  return finish_launch(kvq::launch_dsv4(a, kvq_dsv4_dispatch_path(num_tokens, num_heads),
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_NULL: return "a required pointer is NULL";
+    case KVQ_ERR_SHAPE: return "invalid count or size";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported head_dim / rotary layout";
+    case KVQ_ERR_ALIGN: return "pointer not aligned as required";
+    case KVQ_ERR_CUDA: return "CUDA launch failed (see kvq_last_cuda_error)";
+    case KVQ_ERR_VALUE: return "eps must be finite and non-negative";
+  }
+  return "unknown kvq_status";
+}
+
+int kvq_last_cuda_error(void) { return t_last_cuda_error; }
+
+int64_t kvq_dsv4_dispatch_threshold(void) { return current_threshold(); }
+
+int64_t kvq_set_dsv4_dispatch_threshold(int64_t value) {
+  const int64_t prev = current_threshold();
+  g_threshold.store(value >= 0 ? value : -1, std::memory_order_relaxed);
+  return prev;
+}
+
+int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
+  return num_tokens * (int64_t)(num_heads + 1) < current_threshold() ? 0 : 1;
+}
+
+}  // extern "C"

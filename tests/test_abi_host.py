@@ -1,0 +1,140 @@
+"""The C ABI on the host: symbols, status strings, validation, dispatch.
+
+No call here reaches a kernel launch: every call either fails host-side
+validation (the pointers passed are never dereferenced) or has nothing to do
+(num_tokens == 0).  Runs without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kv_quant_cache_gb300 as kvq
+from kv_quant_cache_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return kvq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_operators():
+    names = declared_functions()
+    for n in ("fused_qk_norm_rope", "dsv4_qnorm_rope_kv_rope_quant_insert", "kvq_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libkvq.so does not export {name}"
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert kvq.status_string(s)
+    assert kvq.status_string(99) == "unknown kvq_status"
+
+
+# fake, never-dereferenced device addresses for validation tests
+A16 = 0x10000
+MIS = 0x10008  # 8-byte but not 16-byte aligned
+
+
+def qk(L, qkv=A16, T=4, hq=2, hk=1, hv=1, d=128, eps=1e-6, qw=A16, kw=A16, cs=A16, neox=1, pos=A16):
+    return L.fused_qk_norm_rope(qkv, T, hq, hk, hv, d, eps, qw, kw, cs, neox, pos, None)
+
+
+def dsv4(L, q=A16, kv=A16, T=4, H=2, eps=1e-6, qw=A16, kvw=A16, cs=A16, pos=A16, slot=A16,
+         cache=A16, bs=64):
+    return L.dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, T, H, eps, qw, kvw, cs, pos, slot, cache,
+                                                  bs, None)
+
+
+def test_qk_validation(L):
+    assert qk(L, qkv=None) == kvq.KVQ_ERR_NULL
+    assert qk(L, pos=None) == kvq.KVQ_ERR_NULL
+    assert qk(L, T=-1) == kvq.KVQ_ERR_SHAPE
+    assert qk(L, hq=-1) == kvq.KVQ_ERR_SHAPE
+    assert qk(L, d=64) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, neox=0) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, eps=-1.0) == kvq.KVQ_ERR_VALUE
+    assert qk(L, eps=float("nan")) == kvq.KVQ_ERR_VALUE
+    assert qk(L, eps=float("inf")) == kvq.KVQ_ERR_VALUE
+    assert qk(L, qkv=MIS) == kvq.KVQ_ERR_ALIGN
+    assert qk(L, cs=MIS) == kvq.KVQ_ERR_ALIGN
+    assert qk(L, pos=A16 + 4) == kvq.KVQ_ERR_ALIGN
+    assert qk(L, T=1 << 30, hq=2, hk=0) == kvq.KVQ_ERR_SHAPE   # index range
+    # nothing to do: OK without a launch, even with NULL pointers
+    assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, T=0) == kvq.KVQ_OK
+    assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, hq=0, hk=0) == kvq.KVQ_OK
+
+
+def test_dsv4_validation(L):
+    assert dsv4(L, q=None) == kvq.KVQ_ERR_NULL
+    assert dsv4(L, slot=None) == kvq.KVQ_ERR_NULL
+    assert dsv4(L, cache=None) == kvq.KVQ_ERR_NULL
+    assert dsv4(L, T=-3) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, H=0) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, bs=0) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, T=1 << 24, H=128) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, eps=float("nan")) == kvq.KVQ_ERR_VALUE
+    assert dsv4(L, q=MIS) == kvq.KVQ_ERR_ALIGN
+    assert dsv4(L, kv=MIS) == kvq.KVQ_ERR_ALIGN
+    assert dsv4(L, qw=MIS) == kvq.KVQ_ERR_ALIGN
+    assert dsv4(L, cache=A16 + 4) == kvq.KVQ_ERR_ALIGN
+    assert dsv4(L, q=None, kv=None, qw=None, kvw=None, cs=None, pos=None, slot=None, cache=None,
+                T=0) == kvq.KVQ_OK
+
+
+def test_cache_alignment_rule_is_eight_bytes(L):
+    # an 8-byte aligned cache passes alignment; make another argument invalid so
+    # that nothing launches, and check that the reported error is not ALIGN.
+    assert dsv4(L, cache=A16 + 8, bs=0) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, cache=A16 + 8, slot=None) == kvq.KVQ_ERR_NULL
+
+
+def test_dispatch_threshold(L):
+    old = kvq.set_dsv4_dispatch_threshold(-1)
+    try:
+        default = kvq.dsv4_dispatch_threshold()
+        assert default > 0
+        assert kvq.dsv4_dispatch_path(1, 128) == 0
+        assert kvq.dsv4_dispatch_path(131072, 128) == 1
+        kvq.set_dsv4_dispatch_threshold(0)
+        assert kvq.dsv4_dispatch_path(1, 1) == 1
+        kvq.set_dsv4_dispatch_threshold(1 << 40)
+        assert kvq.dsv4_dispatch_path(131072, 128) == 0
+        assert kvq.set_dsv4_dispatch_threshold(-1) == 1 << 40
+        assert kvq.dsv4_dispatch_threshold() == default
+        # the boundary is a program count T * (H + 1)
+        kvq.set_dsv4_dispatch_threshold(129 * 4)
+        assert kvq.dsv4_dispatch_path(3, 128) == 0 and kvq.dsv4_dispatch_path(4, 128) == 1
+    finally:
+        kvq.set_dsv4_dispatch_threshold(old)
+
+
+def test_binding_rejects_cpu_tensors(L):
+    import torch
+    x = torch.zeros(2, 4 * 128, dtype=torch.bfloat16)
+    w = torch.zeros(128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kvq.fused_qk_norm_rope(x, 2, 1, 1, 128, 1e-6, w, w, torch.zeros(4, 128), True,
+                               torch.zeros(2, dtype=torch.int64))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(kvq, "_LIB", None)
+    monkeypatch.setattr(kvq, "LIB_PATH", str(tmp_path / "libkvq.so"))
+    with pytest.raises(kvq.KvqError):
+        kvq.lib()

@@ -1,0 +1,138 @@
+"""dsv4_qnorm_rope_kv_rope_quant_insert on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import kv_quant_cache_gb300 as kvq
+import workloads as wl
+from gpu_cases import SMALL_PATH, TILED_PATH, dsv4_parity, run_dsv4, to_device, with_threshold
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("threshold", [None, SMALL_PATH, TILED_PATH], ids=["auto", "small", "tiled"])
+def test_decode_size_16_tokens(cuda_device, threshold):
+    d = wl.make_dsv4_workload(wl.DSV4_DECODE, device=cuda_device)
+    assert int((d["slot_mapping"] < 0).sum()) == 2
+    if threshold is None:
+        qrep, crep = dsv4_parity(d)
+    else:
+        with with_threshold(threshold):
+            qrep, crep = dsv4_parity(d)
+    assert crep.entries == 14
+    assert crep.exp_mismatch_ties == 0
+
+
+def test_prefill_32768x64_every_token(cuda_device):
+    """The benchmarked workload (default dispatch = token-tiled launch), every
+    token and the whole cache compared."""
+    d = wl.make_dsv4_workload(wl.DSV4_LARGE, device=cuda_device)
+    assert kvq.dsv4_dispatch_path(32768, 64) == 1
+    qrep, crep = dsv4_parity(d, slice_tokens=1024)
+    assert qrep.n == 32768 * 64 * 512
+    assert crep.entries == 32768
+    print(f"q exact {qrep.exact_frac:.5f}; codes exact {crep.codes_exact / crep.codes:.7f}; "
+          f"exponent near-ties {crep.exp_mismatch_ties}")
+
+
+@pytest.mark.parametrize("w", [w for w in wl.DSV4_SWEEP if w.T <= 8192], ids=lambda w: w.name)
+def test_sweep_every_token(cuda_device, w):
+    dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), slice_tokens=512)
+
+
+@pytest.mark.parametrize("w", [w for w in wl.DSV4_SWEEP if w.T > 8192], ids=lambda w: w.name)
+def test_sweep_full_size_sampled(cuda_device, w):
+    """Full-size launch; 1024 sampled tokens (plus the first and last 8) compared
+    with the oracle, and the whole cache checked for untouched slots."""
+    dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), sample=1024, seed=w.seed)
+
+
+@pytest.mark.parametrize("T", [1, 4, 17, 511, 512, 777, 1000])
+@pytest.mark.parametrize("threshold", [SMALL_PATH, TILED_PATH], ids=["small", "tiled"])
+@pytest.mark.parametrize("H", [1, 3, 64])
+def test_ragged_both_launches(cuda_device, T, threshold, H):
+    """Token counts off every tile and odd head counts, forced through each launch."""
+    d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 16), block_size=16,
+                     slots="distinct_skip2", seed=100 + T + H, device=cuda_device)
+    with with_threshold(threshold):
+        dsv4_parity(d)
+
+
+def test_all_tokens_unmapped(cuda_device):
+    d = wl.make_dsv4(37, 2, max_pos=1024, num_blocks=4, block_size=16, seed=7, device=cuda_device)
+    d["slot_mapping"].fill_(-1)
+    qrep, crep = dsv4_parity(d)
+    assert crep.entries == 0
+
+
+def test_last_slot_and_last_position(cuda_device):
+    d = wl.make_dsv4(4, 2, max_pos=4096, num_blocks=3, block_size=8, seed=8, device=cuda_device)
+    d["slot_mapping"] = torch.tensor([23, 0, -1, 22], dtype=torch.int64, device=cuda_device)
+    d["positions"] = torch.tensor([4095, 0, 4095, 1], dtype=torch.int64, device=cuda_device)
+    dsv4_parity(d)
+
+
+def _exact_case(block_w, T=3):
+    """kv = q = +-1, eps = 0, position 0: r = 1 exactly and the rotation is the
+    identity, so n = +-w exactly in fp32 and fp64, and every exponent and code
+    decision is exact on both sides."""
+    rng = np.random.default_rng(3)
+    d = wl.make_dsv4(T, 2, max_pos=4, num_blocks=2, block_size=8, seed=4, device="cpu", eps=0.0)
+    d["q"] = wl.bf16_from_values(np.where(rng.random((T, 2, 512)) < 0.5, -1.0, 1.0))
+    d["kv"] = wl.bf16_from_values(np.where(rng.random((T, 512)) < 0.5, -1.0, 1.0))
+    d["kv_weight"] = wl.bf16_from_values(block_w)
+    d["positions"] = torch.zeros(T, dtype=torch.int64)
+    return d
+
+
+def test_exponent_boundaries_and_code_ties_exact(cuda_device):
+    # block 0: amax exactly 448 * 2^-7 = 3.5 (e = -7, not -6); block 1: one bf16
+    # step above 3.5 (e = -6); block 2: e4m3 midpoints after scaling (ties to
+    # even); block 3: values whose scaled codes are subnormal e4m3; block 4:
+    # a block of zeros (byte 0); blocks 5, 6: mixed powers of two; rotary dims.
+    w = np.ones(512)
+    w[0:64] = 3.5
+    w[1:64:2] = -1.25
+    w[64:128] = 3.515625
+    w[128:192] = [1.0 + 1.0 / 16 * (k % 8) for k in range(64)]  # 17/16.. -> ties at 2^-e scale
+    w[128] = 2.0 ** 3
+    w[192:256] = [(k % 8 + 0.5) * 2.0 ** -17 for k in range(64)]  # subnormal e4m3 ties
+    w[192] = 1.0
+    w[256:320] = 0.0
+    w[320:384] = [2.0 ** (k % 9 - 4) for k in range(64)]
+    w[384:448] = [-(2.0 ** (-(k % 11))) for k in range(64)]
+    w[448:512] = np.linspace(-2, 2, 64)
+    d = to_device(_exact_case(w), cuda_device)
+    qrep, crep = dsv4_parity(d)
+    assert qrep.exact == qrep.n
+    assert crep.codes_exact == crep.codes and crep.exp_mismatch_ties == 0
+    assert crep.rope.exact == crep.rope.n
+    ent = d["kv_cache"].view(-1, 584)[d["slot_mapping"][0]].cpu().numpy()
+    assert ent[576] == 120 and ent[577] == 121 and ent[580] == 0
+
+
+def test_zero_kv_vector(cuda_device):
+    d = wl.make_dsv4(5, 2, max_pos=64, num_blocks=2, block_size=8, seed=9, device="cpu")
+    d["kv"][1:3] = 0
+    d = to_device(d, cuda_device)
+    dsv4_parity(d)
+    ent = d["kv_cache"].view(-1, 584)[d["slot_mapping"][1]].cpu().numpy()
+    assert np.all(ent[576:583] == 0) and np.all((ent[:448] & 0x7F) == 0)
+
+
+def test_zero_tokens_is_a_no_op(cuda_device):
+    d = wl.make_dsv4(0, 4, num_blocks=1, block_size=4, device=cuda_device)
+    before = d["kv_cache"].clone()
+    run_dsv4(d)
+    torch.cuda.synchronize()
+    assert torch.equal(before, d["kv_cache"])
+
+
+def test_repeat_calls_are_deterministic(cuda_device):
+    d = wl.make_dsv4(300, 8, max_pos=4096, num_blocks=16, block_size=64, seed=12,
+                     device=cuda_device)
+    d2 = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    run_dsv4(d)
+    run_dsv4(d2)
+    torch.cuda.synchronize()
+    assert torch.equal(d["q"], d2["q"]) and torch.equal(d["kv_cache"], d2["kv_cache"])

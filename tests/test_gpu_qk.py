@@ -1,0 +1,84 @@
+"""fused_qk_norm_rope on the GPU against the oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import kv_quant_cache_gb300 as kvq
+import workloads as wl
+from gpu_cases import qk_parity, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_size_17_tokens(cuda_device):
+    rep = qk_parity(wl.make_qk_workload(wl.QK_SMALL, device=cuda_device))
+    assert rep.exact_frac > 0.95
+
+
+def test_prefill_32768_tokens_every_token(cuda_device):
+    """The benchmarked workload, compared in full (1,310,720 head rows)."""
+    rep = qk_parity(wl.make_qk_workload(wl.QK_LARGE, device=cuda_device), slice_tokens=8192)
+    assert rep.n == 32768 * 40 * 128
+    assert rep.exact_frac > 0.95
+
+
+@pytest.mark.parametrize("T", [1, 4, 17, 511, 512, 777, 1000, 4096])
+@pytest.mark.parametrize("heads", [(16, 8, 8), (3, 2, 1), (5, 0, 2), (0, 3, 0), (1, 1, 0),
+                                   (32, 8, 8)])
+def test_ragged_shapes(cuda_device, T, heads):
+    """Token counts that are not multiples of any tile, odd Q+K counts, no K,
+    no Q, no V: both launch shapes (the small one below 1216 rows)."""
+    Hq, Hk, Hv = heads
+    d = wl.make_qk(T, Hq, Hk, Hv, theta=1e6, max_pos=131072, seed=T * 7 + Hq,
+                   device=cuda_device)
+    qk_parity(d)
+
+
+def test_positions_at_table_edges(cuda_device):
+    d = wl.make_qk(64, 4, 2, 2, theta=1e4, max_pos=4096, seed=5, device=cuda_device)
+    d["positions"] = torch.tensor([0, 4095] * 32, dtype=torch.int64, device=cuda_device)
+    qk_parity(d)
+
+
+def test_exact_arithmetic_rows(cuda_device):
+    """x = +-1 everywhere, eps = 0 and position 0: r = 1 exactly and the
+    rotation is the identity, so every output is w rounded to bf16 -- bit-exact."""
+    T, Hq, Hk, Hv = 9, 2, 2, 1
+    rng = np.random.default_rng(1)
+    sign = np.where(rng.random((T, (Hq + Hk + Hv) * 128)) < 0.5, -1.0, 1.0)
+    d = wl.make_qk(T, Hq, Hk, Hv, max_pos=8, seed=2, device="cpu", eps=0.0)
+    d["qkv"] = wl.bf16_from_values(sign)
+    d["positions"] = torch.zeros(T, dtype=torch.int64)
+    rep = qk_parity(to_device(d, cuda_device))
+    assert rep.exact == rep.n
+
+
+def test_zero_rows_and_tiny_values(cuda_device):
+    """All-zero heads (r = 1/sqrt(eps)) and values far below 1 stay finite and match."""
+    d = wl.make_qk(16, 4, 4, 0, max_pos=64, seed=3, device="cpu")
+    x = d["qkv"].float()
+    x[0:4] = 0.0
+    x[4:8] *= 1e-30
+    x[8:12] *= 1e6
+    d["qkv"] = x.to(torch.bfloat16)
+    qk_parity(to_device(d, cuda_device))
+
+
+def test_zero_tokens_is_a_no_op(cuda_device):
+    d = wl.make_qk(0, 2, 1, 1, device=cuda_device)
+    kvq.fused_qk_norm_rope(d["qkv"], 2, 1, 1, 128, 1e-6, d["q_weight"], d["k_weight"],
+                           d["cos_sin"], True, d["positions"])
+    torch.cuda.synchronize()
+
+
+def test_runs_on_a_side_stream(cuda_device):
+    d = wl.make_qk(300, 8, 4, 4, max_pos=4096, seed=9, device=cuda_device)
+    s = torch.cuda.Stream(cuda_device)
+    ref = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        kvq.fused_qk_norm_rope(d["qkv"], 8, 4, 4, 128, 1e-6, d["q_weight"], d["k_weight"],
+                               d["cos_sin"], True, d["positions"], stream=s)
+    s.synchronize()
+    qk_parity(ref)  # the same inputs through the default stream
+    assert torch.equal(d["qkv"], ref["qkv"])

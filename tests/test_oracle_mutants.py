@@ -45,7 +45,8 @@ MUTANTS = {
                               "entry[DSV4_ROPE_AT + 2 * i] = (uint8_t)(bits >> 8);"),
     "amax_wrong_block": ("double v = n[b * DSV4_BLOCK + j];", "double v = n[b * DSV4_BLOCK + j + 1];"),
     "codes_unscaled": ("orc_e4m3_encode(ldexp((double)f[j], -e))", "orc_e4m3_encode((double)f[j])"),
-    "slot_hardcoded_block": ("(blk * A->block_size + off)", "(blk * 64 + off)"),
+    # (kept inside the cache: a mutant must not write out of bounds)
+    "slot_hardcoded_block": ("(blk * A->block_size + off)", "((blk * 64 + off) % A->num_slots)"),
     "skip_ignored": ("const int64_t s = A->slot[t];", "const int64_t s = A->slot[t] < 0 ? 0 : A->slot[t];"),
     "kv_uses_q_weight": ("rms_norm_weight(A->kv + krow, A->kvw,", "rms_norm_weight(A->kv + krow, A->qw,"),
 }
