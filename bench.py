@@ -274,28 +274,28 @@ def time_e2e(kvq, qk, ds, steps, device):
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
-def cpu_baseline(sample_tokens=4096):
-    """The oracle as it stands, all host cores, on the first `sample_tokens`
-    tokens of both workloads of the step (inputs generated on the CPU with the
-    same recipe).  Returns (GB/s by the same byte count, threads, description)."""
+def host_step_inputs(qk, ds):
+    """Host copies of the step's inputs (bf16 as uint16 bits) for the oracle."""
+    def h(t):
+        return wl.bf16_bits(t) if t.dtype == torch.bfloat16 else wl.host(t)
+    return ({k: h(v) for k, v in qk.items() if isinstance(v, torch.Tensor)},
+            {k: h(v) for k, v in ds.items() if isinstance(v, torch.Tensor)})
+
+
+def cpu_baseline(qk, ds, qk_h, ds_h):
+    """The oracle as it stands, all host cores, on the whole step's inputs
+    (both operators, all 32768 tokens).  Returns (GB/s by the same byte
+    count, threads, seconds)."""
     import oracle
-    qk = wl.make_qk(sample_tokens, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001)
-    ds = wl.make_dsv4(sample_tokens, 64, max_pos=131072, num_blocks=1024, block_size=64,
-                      slots="perm_prefix", seed=1003)
-    qk_in = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
-             for k, v in qk.items() if isinstance(v, torch.Tensor)}
-    ds_in = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
-             for k, v in ds.items() if isinstance(v, torch.Tensor)}
-    cache = ds_in["kv_cache"].copy()
+    cache = ds_h["kv_cache"].copy()
     t0 = time.perf_counter()
-    oracle.qk_norm_rope(qk_in["qkv"], 32, 8, 8, 128, qk["eps"], qk_in["q_weight"],
-                        qk_in["k_weight"], qk_in["cos_sin"], qk_in["positions"])
-    oracle.dsv4(ds_in["q"], ds_in["kv"], ds["eps"], ds_in["q_weight"], ds_in["kv_weight"],
-                ds_in["cos_sin"], ds_in["positions"], ds_in["slot_mapping"], cache)
+    oracle.qk_norm_rope(qk_h["qkv"], qk["Hq"], qk["Hk"], qk["Hv"], qk["D"], qk["eps"],
+                        qk_h["q_weight"], qk_h["k_weight"], qk_h["cos_sin"], qk_h["positions"])
+    oracle.dsv4(ds_h["q"], ds_h["kv"], ds["eps"], ds_h["q_weight"], ds_h["kv_weight"],
+                ds_h["cos_sin"], ds_h["positions"], ds_h["slot_mapping"], cache)
     dt = time.perf_counter() - t0
-    nbytes = qk_bytes(sample_tokens, 32, 8) + dsv4_bytes(sample_tokens, 64, sample_tokens)
-    return nbytes / dt / 1e9, oracle.default_threads(), dt, (
-        f"first {sample_tokens} of 32768 tokens of both operators of the step (fp64 oracle)")
+    b_qk, b_ds = step_bytes(qk, ds)
+    return (b_qk + b_ds) / dt / 1e9, oracle.default_threads(), dt
 
 
 def config_block(extra=None):
@@ -316,6 +316,9 @@ def run_gpu(args):
     kvq.lib()
     qk, ds = make_step_inputs(device)
     b_qk, b_ds = step_bytes(qk, ds)
+    host_inputs = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_inputs = host_step_inputs(qk, ds)
     warmup = max(args.warmup, 3)
     clocks = ClockSampler(local)
     total_ms, qk_ms, ds_ms = time_device(kvq, qk, ds, args.steps, warmup, world, device)
@@ -337,10 +340,12 @@ def run_gpu(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "steps": e2e_steps}
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, dt, sample = cpu_baseline(args.cpu_sample_tokens)
+    if host_inputs is not None:
+        v, cores, dt = cpu_baseline(qk, ds, *host_inputs)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": sample, "seconds": round(dt, 2)}
+               "sample": "one whole step (both operators, all 32768 tokens, the same input "
+                         "bytes as the GPU step), fp64 oracle, all host cores",
+               "seconds": round(dt, 2)}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 5),
@@ -349,9 +354,11 @@ def run_gpu(args):
             "algorithmic_bytes_per_step": b_qk + b_ds, "qk_bytes": b_qk, "dsv4_bytes": b_ds,
             "qk_ms": round(qk_avg, 5), "dsv4_ms": round(ds_avg, 5),
             "qk_gbs": round(b_qk / (qk_avg * 1e-3) / 1e9, 1),
+            "qk_kernel": kvq.configs("qk")[kvq.qk_config_for(32768, 32, 8)],
             "pct_of_peak": round(100 * value / world / peak, 2),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": "hbm", "kernel": "dsv4_kernel<8,4,1> (token-tiled)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "dsv4 " + kvq.configs("dsv4")[kvq.dsv4_config_for(32768, 64)],
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": b_ds},
@@ -439,62 +446,64 @@ def _time_launch(fn, reps, stream, flush=None):
 
 
 def sweep(kvq, device):
+    """Every workload under every launch configuration, the DSV4 dispatch
+    crossover, and a 512 MiB device-to-device copy ceiling (JSON lines on
+    stderr)."""
     peak, _ = peak_hbm()
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
     out = []
-    # device-to-device copy ceiling (counting read + write)
+
+    def emit(rec):
+        out.append(rec)
+        sys.stderr.write(json.dumps(rec) + "\n")
+        sys.stderr.flush()
+
     src = torch.empty(512 * 2**20, dtype=torch.uint8, device=device)
     dst = torch.empty_like(src)
     med, best = _time_launch(lambda: dst.copy_(src), 20, stream)
-    out.append({"sweep": "d2d_copy_512MiB", "gbs_median": round(2 * src.numel() / med / 1e6, 1),
-                "gbs_best": round(2 * src.numel() / best / 1e6, 1)})
+    emit({"sweep": "d2d_copy_512MiB", "gbs_median": round(2 * src.numel() / med / 1e6, 1),
+          "gbs_best": round(2 * src.numel() / best / 1e6, 1)})
     del src, dst
+
+    def run_configs(op, name, nb, fn, reps):
+        small = nb < 256 * 2**20
+        auto = None
+        for cid, cname in [(-1, "auto")] + list(enumerate(kvq.configs(op))):
+            old = kvq.set_config(op, cid)
+            try:
+                med, _ = _time_launch(fn, reps, stream, flush if small else None)
+            finally:
+                kvq.set_config(op, old)
+            emit({"sweep": name, "config": cname, "bytes": nb, "us_median": round(med * 1e3, 2),
+                  "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
+                  "l2_flush": small})
+
     for w in (wl.QK_SMALL, wl.QK_LARGE):
         d = wl.make_qk_workload(w, device=device)
-        nb = qk_bytes(w.T, w.Hq, w.Hk)
-        small = nb < 256 * 2**20
-        med, best = _time_launch(lambda: launch_qk(kvq, d, stream), 50, stream,
-                                 flush if small else None)
-        out.append({"sweep": w.name, "bytes": nb, "us_median": round(med * 1e3, 2),
-                    "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
-                    "l2_flush": small})
+        run_configs("qk", w.name, qk_bytes(w.T, w.Hq, w.Hk), lambda: launch_qk(kvq, d, stream), 30)
         del d
-    ds_work = [wl.DSV4_DECODE, wl.DSV4_LARGE, *wl.DSV4_SWEEP]
-    for w in ds_work:
+    for w in [wl.DSV4_DECODE, wl.DSV4_LARGE, *wl.DSV4_SWEEP]:
         d = wl.make_dsv4_workload(w, device=device)
-        mapped = int((d["slot_mapping"] >= 0).sum())
-        nb = dsv4_bytes(w.T, w.H, mapped)
-        small = nb < 256 * 2**20
-        for path, thr in (("auto", -1), ("small", 1 << 40), ("tiled", 0)):
-            old = kvq.set_dsv4_dispatch_threshold(thr)
-            try:
-                med, best = _time_launch(lambda: launch_dsv4(kvq, d, stream),
-                                         50 if nb < 2**30 else 15, stream, flush if small else None)
-            finally:
-                kvq.set_dsv4_dispatch_threshold(old)
-            out.append({"sweep": w.name, "path": path, "bytes": nb, "us_median": round(med * 1e3, 2),
-                        "gbs": round(nb / med / 1e6, 1),
-                        "pct_peak": round(100 * nb / med / 1e6 / peak, 1), "l2_flush": small})
+        nb = dsv4_bytes(w.T, w.H, int((d["slot_mapping"] >= 0).sum()))
+        run_configs("dsv4", w.name, nb, lambda: launch_dsv4(kvq, d, stream), 30 if nb < 2**32 else 8)
         del d
-    # dispatch crossover: program count T * (H + 1) at which tiled starts to win
+    # dispatch crossover between the small- and large-batch shapes
     for H in (64, 128):
-        for T in (1, 2, 4, 8, 16, 32, 64, 128, 192, 256, 384, 512, 1024):
+        for T in (1, 4, 16, 64, 128, 256, 512, 1024, 4096):
             d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 64), block_size=64,
                              seed=7 + T, device=device)
             res = {}
-            for path, thr in (("small", 1 << 40), ("tiled", 0)):
+            for path, thr in (("small", 1 << 40), ("large", 0)):
                 old = kvq.set_dsv4_dispatch_threshold(thr)
                 try:
-                    res[path] = _time_launch(lambda: launch_dsv4(kvq, d, stream), 50, stream, flush)[0]
+                    res[path] = _time_launch(lambda: launch_dsv4(kvq, d, stream), 30, stream, flush)[0]
                 finally:
                     kvq.set_dsv4_dispatch_threshold(old)
-            out.append({"sweep": "dispatch", "T": T, "H": H, "programs": T * (H + 1),
-                        "small_us": round(res["small"] * 1e3, 2), "tiled_us": round(res["tiled"] * 1e3, 2)})
+            emit({"sweep": "dispatch", "T": T, "H": H, "programs": T * (H + 1),
+                  "small_us": round(res["small"] * 1e3, 2), "large_us": round(res["large"] * 1e3, 2)})
             del d
-    for o in out:
-        sys.stderr.write(json.dumps(o) + "\n")
-    sys.stderr.flush()
+    return out
 
 
 def run_profile_case(args):
@@ -521,14 +530,15 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("kvq", "reference"), default="kvq")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096,
+                    help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--profile", choices=("qk", "dsv4"), default=None)
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--heads", type=int, default=64)

@@ -136,8 +136,8 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
  * Other cache bytes are never written.
  *
  * Launch shape: a program count T * (H + 1) below the dispatch threshold
- * (kvq_dsv4_dispatch_threshold) takes the small-batch launch, otherwise the
- * token-tiled one.  Results do not depend on the choice.
+ * (kvq_dsv4_dispatch_threshold) takes the small-batch launch shape, otherwise
+ * the large-batch one.  Results do not depend on the choice.
  */
 kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
     void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
@@ -161,8 +161,32 @@ int64_t kvq_dsv4_dispatch_threshold(void);
  * (value < 0).  Returns the previous threshold.  Not synchronised with
  * concurrent launches on other threads. */
 int64_t kvq_set_dsv4_dispatch_threshold(int64_t value);
-/* Which launch a call with these sizes takes: 0 small-batch, 1 token-tiled. */
+/* Which side of the threshold a call with these sizes falls on: 0 small-batch
+ * launch shape, 1 large-batch launch shape. */
 int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
+
+/*
+ * Launch shapes (diagnostics and tuning).  Each operator has a fixed table of
+ * launch configurations (kernel shape, warps per CTA, rows per warp); every
+ * configuration computes bit-identical results.  The automatic dispatch picks
+ * one by problem size; the override forces one for every later call of the
+ * process (benchmark sweeps, tests).
+ *   *_num_configs   number of configurations
+ *   *_config_name   static name of configuration id (NULL if out of range)
+ *   kvq_set_*_config  force id (0 <= id < num) or restore automatic (id < 0);
+ *                   returns the previous override (-1 = automatic), or -2 and
+ *                   changes nothing if id >= num.  Not synchronised with
+ *                   launches on other threads.
+ *   *_config_for    the configuration a call with these sizes would use now
+ */
+int kvq_qk_num_configs(void);
+const char* kvq_qk_config_name(int id);
+int kvq_set_qk_config(int id);
+int kvq_qk_config_for(int64_t num_tokens, int num_heads_q, int num_heads_k);
+int kvq_dsv4_num_configs(void);
+const char* kvq_dsv4_config_name(int id);
+int kvq_set_dsv4_config(int id);
+int kvq_dsv4_config_for(int64_t num_tokens, int num_heads);
 
 #ifdef __cplusplus
 }

@@ -58,6 +58,17 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.kvq_set_dsv4_dispatch_threshold.argtypes = [_I64]
     L.kvq_dsv4_dispatch_path.restype = _I
     L.kvq_dsv4_dispatch_path.argtypes = [_I64, _I]
+    for op in ("qk", "dsv4"):
+        getattr(L, f"kvq_{op}_num_configs").restype = _I
+        getattr(L, f"kvq_{op}_num_configs").argtypes = []
+        getattr(L, f"kvq_{op}_config_name").restype = ctypes.c_char_p
+        getattr(L, f"kvq_{op}_config_name").argtypes = [_I]
+        getattr(L, f"kvq_set_{op}_config").restype = _I
+        getattr(L, f"kvq_set_{op}_config").argtypes = [_I]
+    L.kvq_qk_config_for.restype = _I
+    L.kvq_qk_config_for.argtypes = [_I64, _I, _I]
+    L.kvq_dsv4_config_for.restype = _I
+    L.kvq_dsv4_config_for.argtypes = [_I64, _I]
     return L
 
 
@@ -157,3 +168,27 @@ def set_dsv4_dispatch_threshold(value: int) -> int:
 
 def dsv4_dispatch_path(num_tokens: int, num_heads: int) -> int:
     return lib().kvq_dsv4_dispatch_path(int(num_tokens), int(num_heads))
+
+
+def configs(op: str) -> list:
+    """Names of the launch configurations of ``op`` ("qk" or "dsv4")."""
+    L = lib()
+    n = getattr(L, f"kvq_{op}_num_configs")()
+    return [getattr(L, f"kvq_{op}_config_name")(i).decode() for i in range(n)]
+
+
+def set_config(op: str, config_id: int) -> int:
+    """Force launch configuration ``config_id`` of ``op`` (< 0: automatic);
+    returns the previous override."""
+    prev = getattr(lib(), f"kvq_set_{op}_config")(int(config_id))
+    if prev == -2:
+        raise ValueError(f"{op}: no launch configuration {config_id}")
+    return prev
+
+
+def qk_config_for(num_tokens: int, num_heads_q: int, num_heads_k: int) -> int:
+    return lib().kvq_qk_config_for(int(num_tokens), int(num_heads_q), int(num_heads_k))
+
+
+def dsv4_config_for(num_tokens: int, num_heads: int) -> int:
+    return lib().kvq_dsv4_config_for(int(num_tokens), int(num_heads))

@@ -11,10 +11,23 @@
 namespace {
 
 // Program-count crossover (T * (H + 1)) between the small-batch and the
-// token-tiled DSV4 launch, measured on GB300 by the benchmark's dispatch sweep.
-constexpr int64_t kDefaultDsv4Threshold = 16384;
+// large-batch DSV4 launch shapes, measured on GB300 by the benchmark's
+// dispatch sweep (the two shapes tie within 2% between 33K and 130K
+// programs; below, the one-row-per-warp grid has the lower latency).
+constexpr int64_t kDefaultDsv4Threshold = 65536;
+// Launch shapes (indices into kDsv4Configs / kQkConfigs) the automatic
+// dispatch uses below / above the threshold.
+constexpr int kDsv4SmallConfig = 0;  // tiles<4w,1row>
+constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg>
+constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
+constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
+// Q+K head rows below which the QK operator takes its small-batch shape.
+constexpr int64_t kQkSmallRows = 152 * 8;
 
 std::atomic<int64_t> g_threshold{-1};
+std::atomic<int> g_dsv4_config{-1};
+std::atomic<int> g_qk_config{-1};
+std::atomic<int> g_sm_count[kvq::kMaxDevices];
 std::once_flag g_env_once;
 int64_t g_env_threshold = -1;
 thread_local int t_last_cuda_error = 0;
@@ -46,7 +59,45 @@ kvq_status finish_launch(cudaError_t e) {
 
 constexpr int64_t kIndexLimit = (int64_t)1 << 31;
 
+int qk_config_for(int64_t num_tokens, int rows) {
+  const int forced = g_qk_config.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced;
+  return num_tokens * (int64_t)rows < kQkSmallRows ? kQkSmallConfig : kQkLargeConfig;
+}
+
+int dsv4_config_for(int64_t num_tokens, int num_heads) {
+  const int forced = g_dsv4_config.load(std::memory_order_relaxed);
+  if (forced >= 0) return forced;
+  return kvq_dsv4_dispatch_path(num_tokens, num_heads) == 0 ? kDsv4SmallConfig
+                                                            : kDsv4LargeConfig;
+}
+
+int set_config(std::atomic<int>& slot, int id, int n) {
+  const int prev = slot.load(std::memory_order_relaxed);
+  if (id >= n) return -2;
+  slot.store(id < 0 ? -1 : id, std::memory_order_relaxed);
+  return prev;
+}
+
 }  // namespace
+
+namespace kvq {
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace kvq
 
 extern "C" {
 
@@ -79,8 +130,8 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
   a.num_heads_k = num_heads_k;
   a.num_heads_v = num_heads_v;
   a.eps = eps;
-  return finish_launch(kvq::launch_qk_norm_rope(
-      a, kvq::qk_path(num_tokens, rows), reinterpret_cast<cudaStream_t>(stream)));
+  return finish_launch(kvq::launch_qk_norm_rope(a, qk_config_for(num_tokens, rows),
+                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
@@ -111,7 +162,7 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
   a.num_tokens = (int)num_tokens;
   a.num_heads = num_heads;
   a.eps = eps;
-  return finish_launch(kvq::launch_dsv4(a, kvq_dsv4_dispatch_path(num_tokens, num_heads),
+  return finish_launch(kvq::launch_dsv4(a, dsv4_config_for(num_tokens, num_heads),
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -140,6 +191,30 @@ int64_t kvq_set_dsv4_dispatch_threshold(int64_t value) {
 
 int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
   return num_tokens * (int64_t)(num_heads + 1) < current_threshold() ? 0 : 1;
+}
+
+int kvq_qk_num_configs(void) { return kvq::kQkNumConfigs; }
+
+const char* kvq_qk_config_name(int id) {
+  return (id >= 0 && id < kvq::kQkNumConfigs) ? kvq::kQkConfigs[id].name : nullptr;
+}
+
+int kvq_set_qk_config(int id) { return set_config(g_qk_config, id, kvq::kQkNumConfigs); }
+
+int kvq_qk_config_for(int64_t num_tokens, int num_heads_q, int num_heads_k) {
+  return qk_config_for(num_tokens, num_heads_q + num_heads_k);
+}
+
+int kvq_dsv4_num_configs(void) { return kvq::kDsv4NumConfigs; }
+
+const char* kvq_dsv4_config_name(int id) {
+  return (id >= 0 && id < kvq::kDsv4NumConfigs) ? kvq::kDsv4Configs[id].name : nullptr;
+}
+
+int kvq_set_dsv4_config(int id) { return set_config(g_dsv4_config, id, kvq::kDsv4NumConfigs); }
+
+int kvq_dsv4_config_for(int64_t num_tokens, int num_heads) {
+  return dsv4_config_for(num_tokens, num_heads);
 }
 
 }  // extern "C"

@@ -23,10 +23,16 @@
 //     and the rotary bf16 values the next 320 bytes, and lane 0 writes the
 //     seven exponent bytes plus the pad as one 8-byte store.  slot * 584 is a
 //     multiple of 8, so every store is naturally aligned.
-// CTAs are slot-type uniform: the first kv_ctas CTAs each take WARPS*KVROWS
-// tokens' KV vectors, the rest take WARPS*QROWS consecutive q head rows, so
-// no warp mixes the light Q work with the heavier KV work.  Within a warp all
-// row loads are issued before any arithmetic.
+// No warp mixes the light Q work with the heavier KV work (the pages'
+// slot-type-uniform programs).  Two kernel shapes:
+//   * tiles:  one-shot grid; the first CTAs take KV vectors (one token per
+//     warp), the rest QROWS consecutive q rows per warp, all loads of a warp
+//     issued before any arithmetic (KV first measured faster than KV CTAs
+//     spread evenly through the grid);
+//   * stream: persistent grid sized to the resident-CTA capacity of the GPU;
+//     every warp first takes its grid-stride share of KV vectors, then of q
+//     rows, with the next row's loads in flight while the current row is
+//     computed and stored (two register buffers).
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -51,7 +57,7 @@ struct Dsv4Params {
   int num_tokens;
   int num_heads;
   int q_rows;   // num_tokens * num_heads
-  int kv_ctas;  // leading CTAs that do KV work
+  int kv_ctas;  // tiles kernel: leading CTAs that do KV work
   float eps;
 };
 
@@ -83,162 +89,183 @@ __device__ __forceinline__ uint2 e4m3x8(const float* v, float scale) {
   return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
-// Load a row's two 16-byte chunks for this lane.
-__device__ __forceinline__ void load_row(const __nv_bfloat16* row, int lane, uint4& a, uint4& b) {
-  a = load_stream(row + 8 * lane);
-  b = load_stream(row + 256 + 8 * lane);
+// One row's data as held by a lane: two 16-byte chunks plus, on the rotary
+// lanes, the token's four cosines and four sines.
+struct RowRegs {
+  uint4 a, b;
+  float4 c, s;
+};
+
+__device__ __forceinline__ void load_row(const Dsv4Params& p, const __nv_bfloat16* row,
+                                         int64_t token, int lane, RowRegs& r) {
+  r.a = load_stream(row + 8 * lane);
+  r.b = load_stream(row + 256 + 8 * lane);
+  if (lane >= kRopeLane) {
+    const int64_t pos = __ldg(p.positions + token);
+    const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + pos * 64);
+    r.c = __ldg(cs + (lane - kRopeLane));
+    r.s = __ldg(cs + 8 + (lane - kRopeLane));
+  }
 }
 
-// Normalise a row held as 16 fp32 per lane: n = x * r * w, r from the
-// warp-wide sum of squares.
-__device__ __forceinline__ void rms_norm_row(float* x, const float* w, float eps) {
+// The lane's 16 weights, kept packed as bf16 (8 registers) and widened where
+// they are used.
+struct Weights {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ Weights load_weights(const __nv_bfloat16* w, int lane) {
+  return {__ldg(reinterpret_cast<const uint4*>(w) + lane),
+          __ldg(reinterpret_cast<const uint4*>(w) + 32 + lane)};
+}
+
+// n = x * r * w with r from the warp-wide sum of squares, then the
+// interleaved rotation of chunk 1 on the rotary lanes.
+__device__ __forceinline__ void norm_rope(const RowRegs& r, const Weights& wp, float eps,
+                                          int lane, float* x) {
+  unpack_bf16x8(r.a, x);
+  unpack_bf16x8(r.b, x + 8);
   float ss = 0.0f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) ss = fmaf(x[k], x[k], ss);
   ss = group_sum<32>(ss);
-  const float r = __frsqrt_rn(ss * (1.0f / kDim) + eps);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) x[k] = x[k] * r * w[k];
-}
-
-// Interleaved rotation of chunk 1 (x[8..15]) for the rotary lanes.
-__device__ __forceinline__ void rope_chunk1(float* x, const float4& c, const float4& s) {
-  const float cc[4] = {c.x, c.y, c.z, c.w};
-  const float ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float e = x[8 + 2 * j], o = x[9 + 2 * j];
-    x[8 + 2 * j] = fmaf(e, cc[j], -o * ss[j]);
-    x[9 + 2 * j] = fmaf(o, cc[j], e * ss[j]);
-  }
-}
-
-__device__ __forceinline__ void load_cos_sin(const Dsv4Params& p, int64_t token, int lane,
-                                             float4& c, float4& s) {
-  const int64_t pos = __ldg(p.positions + token);
-  const float4* row = reinterpret_cast<const float4*>(p.cos_sin + pos * 64);
-  c = __ldg(row + (lane - kRopeLane));
-  s = __ldg(row + 8 + (lane - kRopeLane));
-}
-
-template <int R>
-__device__ __forceinline__ void q_rows(const Dsv4Params& p, int row0, int lane) {
-  uint4 a[R], b[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    a[i] = b[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (row0 + i < p.q_rows) load_row(p.q + (size_t)(row0 + i) * kDim, lane, a[i], b[i]);
-  }
+  const float rs = __frsqrt_rn(ss * (1.0f / kDim) + eps);
   float w[16];
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.q_weight) + lane), w);
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.q_weight) + 32 + lane), w + 8);
-  float4 c[R], s[R];
+  unpack_bf16x8(wp.a, w);
+  unpack_bf16x8(wp.b, w + 8);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) x[k] = x[k] * rs * w[k];
   if (lane >= kRopeLane) {
+    const float cc[4] = {r.c.x, r.c.y, r.c.z, r.c.w};
+    const float sn[4] = {r.s.x, r.s.y, r.s.z, r.s.w};
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      c[i] = s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (row0 + i < p.q_rows) load_cos_sin(p, (row0 + i) / p.num_heads, lane, c[i], s[i]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    if (row0 + i >= p.q_rows) break;  // warp-uniform
-    float x[16];
-    unpack_bf16x8(a[i], x);
-    unpack_bf16x8(b[i], x + 8);
-    rms_norm_row(x, w, p.eps);
-    if (lane >= kRopeLane) rope_chunk1(x, c[i], s[i]);
-    __nv_bfloat16* row = p.q + (size_t)(row0 + i) * kDim;
-    store_stream(row + 8 * lane, pack_bf16x8(x));
-    store_stream(row + 256 + 8 * lane, pack_bf16x8(x + 8));
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void kv_rows(const Dsv4Params& p, int t0, int lane) {
-  uint4 a[R], b[R];
-  int64_t slot[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    a[i] = b[i] = make_uint4(0u, 0u, 0u, 0u);
-    slot[i] = -1;
-    if (t0 + i < p.num_tokens) {
-      load_row(p.kv + (size_t)(t0 + i) * kDim, lane, a[i], b[i]);
-      slot[i] = __ldg(p.slot_mapping + t0 + i);
-    }
-  }
-  float w[16];
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.kv_weight) + lane), w);
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.kv_weight) + 32 + lane), w + 8);
-  float4 c[R], s[R];
-  if (lane >= kRopeLane) {
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      c[i] = s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t0 + i < p.num_tokens) load_cos_sin(p, t0 + i, lane, c[i], s[i]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    if (t0 + i >= p.num_tokens) break;  // warp-uniform
-    float x[16];
-    unpack_bf16x8(a[i], x);
-    unpack_bf16x8(b[i], x + 8);
-    rms_norm_row(x, w, p.eps);
-    const bool rope_lane = lane >= kRopeLane;
-    if (rope_lane) rope_chunk1(x, c[i], s[i]);
-
-    // Block amax: chunk 0 -> blocks 0..3, chunk 1 -> blocks 4..6 (lanes < 24).
-    float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      m0 = fmaxf(m0, fabsf(x[k]));
-      m1 = fmaxf(m1, fabsf(x[8 + k]));
-    }
-    m0 = group_max<8>(m0);
-    m1 = group_max<8>(m1);
-    const int e0 = ue8m0_byte(m0);
-    const int e1 = ue8m0_byte(m1);
-    const uint2 codes0 = e4m3x8(x, ue8m0_inverse_scale(e0));
-    const uint2 codes1 = e4m3x8(x + 8, ue8m0_inverse_scale(e1));
-    const uint4 rope = pack_bf16x8(x + 8);
-    // Exponent bytes of blocks 0..6 gathered to lane 0.
-    const uint32_t g0 = __shfl_sync(kFullMask, e0, 0), g1 = __shfl_sync(kFullMask, e0, 8);
-    const uint32_t g2 = __shfl_sync(kFullMask, e0, 16), g3 = __shfl_sync(kFullMask, e0, 24);
-    const uint32_t g4 = __shfl_sync(kFullMask, e1, 0), g5 = __shfl_sync(kFullMask, e1, 8);
-    const uint32_t g6 = __shfl_sync(kFullMask, e1, 16);
-
-    if (slot[i] < 0) continue;  // warp-uniform: no cache slot for this token
-    uint8_t* ent = p.kv_cache + slot[i] * kEntry;
-    *reinterpret_cast<uint2*>(ent + 8 * lane) = codes0;
-    if (!rope_lane) {
-      *reinterpret_cast<uint2*>(ent + 256 + 8 * lane) = codes1;
-    } else {
-      uint2* dst = reinterpret_cast<uint2*>(ent + kRopeAt + 16 * (lane - kRopeLane));
-      dst[0] = make_uint2(rope.x, rope.y);
-      dst[1] = make_uint2(rope.z, rope.w);
-    }
-    if (lane == 0) {
-      *reinterpret_cast<uint2*>(ent + kScaleAt) =
-          make_uint2(g0 | (g1 << 8) | (g2 << 16) | (g3 << 24), g4 | (g5 << 8) | (g6 << 16));
+    for (int j = 0; j < 4; ++j) {
+      const float e = x[8 + 2 * j], o = x[9 + 2 * j];
+      x[8 + 2 * j] = fmaf(e, cc[j], -o * sn[j]);
+      x[9 + 2 * j] = fmaf(o, cc[j], e * sn[j]);
     }
   }
 }
 
-template <int WARPS, int QROWS, int KVROWS>
-__global__ void __launch_bounds__(WARPS * 32)
-dsv4_kernel(const Dsv4Params p) {
+__device__ __forceinline__ void q_row(const Dsv4Params& p, int row, const RowRegs& r,
+                                      const Weights& w, int lane) {
+  float x[16];
+  norm_rope(r, w, p.eps, lane, x);
+  __nv_bfloat16* dst = p.q + (size_t)row * kDim;
+  store_stream(dst + 8 * lane, pack_bf16x8(x));
+  store_stream(dst + 256 + 8 * lane, pack_bf16x8(x + 8));
+}
+
+__device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, const RowRegs& r,
+                                         const Weights& w, int lane) {
+  float x[16];
+  norm_rope(r, w, p.eps, lane, x);
+  // Block amax: chunk 0 -> blocks 0..3, chunk 1 -> blocks 4..6 (lanes < 24).
+  float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    m0 = fmaxf(m0, fabsf(x[k]));
+    m1 = fmaxf(m1, fabsf(x[8 + k]));
+  }
+  m0 = group_max<8>(m0);
+  m1 = group_max<8>(m1);
+  const int e0 = ue8m0_byte(m0);
+  const int e1 = ue8m0_byte(m1);
+  const uint2 codes0 = e4m3x8(x, ue8m0_inverse_scale(e0));
+  const uint2 codes1 = e4m3x8(x + 8, ue8m0_inverse_scale(e1));
+  const uint4 rope = pack_bf16x8(x + 8);
+  // Exponent bytes of blocks 0..6 gathered to lane 0.
+  const uint32_t g0 = __shfl_sync(kFullMask, e0, 0), g1 = __shfl_sync(kFullMask, e0, 8);
+  const uint32_t g2 = __shfl_sync(kFullMask, e0, 16), g3 = __shfl_sync(kFullMask, e0, 24);
+  const uint32_t g4 = __shfl_sync(kFullMask, e1, 0), g5 = __shfl_sync(kFullMask, e1, 8);
+  const uint32_t g6 = __shfl_sync(kFullMask, e1, 16);
+  if (slot < 0) return;  // warp-uniform: the token has no cache slot
+  uint8_t* ent = p.kv_cache + slot * kEntry;
+  *reinterpret_cast<uint2*>(ent + 8 * lane) = codes0;
+  if (lane < kRopeLane) {
+    *reinterpret_cast<uint2*>(ent + 256 + 8 * lane) = codes1;
+  } else {
+    uint2* dst = reinterpret_cast<uint2*>(ent + kRopeAt + 16 * (lane - kRopeLane));
+    dst[0] = make_uint2(rope.x, rope.y);
+    dst[1] = make_uint2(rope.z, rope.w);
+  }
+  if (lane == 0) {
+    *reinterpret_cast<uint2*>(ent + kScaleAt) =
+        make_uint2(g0 | (g1 << 8) | (g2 << 16) | (g3 << 24), g4 | (g5 << 8) | (g6 << 16));
+  }
+}
+
+// ---- tiles: one-shot grid -------------------------------------------------
+
+template <int WARPS, int QROWS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+dsv4_tiles_kernel(const Dsv4Params p) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if ((int)blockIdx.x < p.kv_ctas) {
-    kv_rows<KVROWS>(p, ((int)blockIdx.x * WARPS + warp) * KVROWS, lane);
-  } else {
-    q_rows<QROWS>(p, (((int)blockIdx.x - p.kv_ctas) * WARPS + warp) * QROWS, lane);
+    const int t = (int)blockIdx.x * WARPS + warp;
+    if (t >= p.num_tokens) return;
+    RowRegs r;
+    load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
+    const int64_t slot = __ldg(p.slot_mapping + t);
+    kv_token(p, slot, r, load_weights(p.kv_weight, lane), lane);
+    return;
+  }
+  const int row0 = (((int)blockIdx.x - p.kv_ctas) * WARPS + warp) * QROWS;
+  RowRegs r[QROWS];
+#pragma unroll
+  for (int i = 0; i < QROWS; ++i)
+    if (row0 + i < p.q_rows)
+      load_row(p, p.q + (size_t)(row0 + i) * kDim, (row0 + i) / p.num_heads, lane, r[i]);
+  const Weights w = load_weights(p.q_weight, lane);
+#pragma unroll
+  for (int i = 0; i < QROWS; ++i) {
+    if (row0 + i >= p.q_rows) break;  // warp-uniform
+    q_row(p, row0 + i, r[i], w, lane);
   }
 }
 
-template <int WARPS, int QROWS, int KVROWS>
-cudaError_t launch(const Dsv4Args& a, cudaStream_t stream) {
+// ---- stream: persistent grid, two-deep register pipeline ------------------
+
+template <int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+dsv4_stream_kernel(const Dsv4Params p) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = (int)gridDim.x * WARPS;
+  Weights w;
+
+  // KV vectors first: each warp's share is small and the heavier per-token
+  // work then overlaps with other warps' q streaming.
+  if (gw < p.num_tokens) {
+    w = load_weights(p.kv_weight, lane);
+    for (int t = gw; t < p.num_tokens; t += nw) {
+      RowRegs r;
+      load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
+      kv_token(p, __ldg(p.slot_mapping + t), r, w, lane);
+    }
+  }
+
+  int row = gw;
+  if (row >= p.q_rows) return;
+  w = load_weights(p.q_weight, lane);
+  RowRegs r0, r1;
+  load_row(p, p.q + (size_t)row * kDim, row / p.num_heads, lane, r0);
+  while (true) {
+    int next = row + nw;
+    if (next < p.q_rows) load_row(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r1);
+    q_row(p, row, r0, w, lane);
+    if (next >= p.q_rows) break;
+    row = next;
+    next = row + nw;
+    if (next < p.q_rows) load_row(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r0);
+    q_row(p, row, r1, w, lane);
+    if (next >= p.q_rows) break;
+    row = next;
+  }
+}
+
+Dsv4Params make_params(const Dsv4Args& a) {
   Dsv4Params p;
   p.q = static_cast<__nv_bfloat16*>(a.q);
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
@@ -251,18 +278,52 @@ cudaError_t launch(const Dsv4Args& a, cudaStream_t stream) {
   p.num_tokens = a.num_tokens;
   p.num_heads = a.num_heads;
   p.q_rows = a.num_tokens * a.num_heads;
+  p.kv_ctas = 0;
   p.eps = a.eps;
-  p.kv_ctas = (a.num_tokens + WARPS * KVROWS - 1) / (WARPS * KVROWS);
+  return p;
+}
+
+template <int WARPS, int QROWS, int MINB>
+cudaError_t launch_tiles(const Dsv4Args& a, cudaStream_t stream) {
+  Dsv4Params p = make_params(a);
+  p.kv_ctas = (p.num_tokens + WARPS - 1) / WARPS;
   const int q_ctas = (p.q_rows + WARPS * QROWS - 1) / (WARPS * QROWS);
-  dsv4_kernel<WARPS, QROWS, KVROWS><<<p.kv_ctas + q_ctas, WARPS * 32, 0, stream>>>(p);
+  dsv4_tiles_kernel<WARPS, QROWS, MINB><<<p.kv_ctas + q_ctas, WARPS * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int WARPS, int MINB>
+cudaError_t launch_stream(const Dsv4Args& a, cudaStream_t stream) {
+  Dsv4Params p = make_params(a);
+  int per_sm = 0;
+  cudaError_t e = resident_ctas(dsv4_stream_kernel<WARPS, MINB>, WARPS * 32, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t work_warps = p.q_rows > p.num_tokens ? p.q_rows : p.num_tokens;
+  int64_t grid = (int64_t)per_sm * device_sm_count();
+  const int64_t need = (work_warps + WARPS - 1) / WARPS;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  dsv4_stream_kernel<WARPS, MINB><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_dsv4(const Dsv4Args& a, int path, cudaStream_t stream) {
-  if (path == 0) return launch<4, 1, 1>(a, stream);
-  return launch<8, 4, 1>(a, stream);
+const LaunchConfig kDsv4Configs[] = {
+    {"tiles<4w,1row>"}, {"tiles<8w,1row>"}, {"tiles<8w,2row>"},
+    {"tiles<8w,4row>"}, {"stream<8w,85reg>"},
+};
+const int kDsv4NumConfigs = sizeof(kDsv4Configs) / sizeof(kDsv4Configs[0]);
+
+cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream) {
+  switch (config) {
+    case 0: return launch_tiles<4, 1, 1>(a, stream);
+    case 1: return launch_tiles<8, 1, 1>(a, stream);
+    case 2: return launch_tiles<8, 2, 4>(a, stream);
+    case 3: return launch_tiles<8, 4, 1>(a, stream);
+    case 4: return launch_stream<8, 3>(a, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

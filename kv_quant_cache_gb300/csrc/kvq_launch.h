@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace kvq {
 
 struct QkArgs {
@@ -32,10 +34,46 @@ struct Dsv4Args {
   float eps;
 };
 
-// Launch shapes.  0 = small batch (one row per warp, narrow CTAs, widest
-// spread over the SMs), 1 = token-tiled (several rows per warp, wide CTAs).
-int qk_path(int64_t num_tokens, int num_rows_per_token);
-cudaError_t launch_qk_norm_rope(const QkArgs& a, int path, cudaStream_t stream);
-cudaError_t launch_dsv4(const Dsv4Args& a, int path, cudaStream_t stream);
+// A launch shape of one operator (an instantiation of one of its kernels).
+struct LaunchConfig {
+  const char* name;
+};
+
+extern const LaunchConfig kQkConfigs[];
+extern const int kQkNumConfigs;
+extern const LaunchConfig kDsv4Configs[];
+extern const int kDsv4NumConfigs;
+
+cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream);
+cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream);
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+constexpr int kMaxDevices = 64;
+
+// CTAs of `kernel` that fit on one SM at `threads` threads per CTA, cached
+// per kernel and device (the occupancy query is not free on every launch).
+template <typename Kernel>
+cudaError_t resident_ctas(Kernel kernel, int threads, int* out) {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *out = v;
+      return cudaSuccess;
+    }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0);
+  if (e != cudaSuccess) return e;
+  if (n < 1) n = 1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  *out = n;
+  return cudaSuccess;
+}
 
 }  // namespace kvq

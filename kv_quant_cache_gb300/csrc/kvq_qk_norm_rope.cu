@@ -7,17 +7,23 @@
 // its own dimension's weight.  This build covers the guarded case of "Notes
 // for Reviewers": bf16, D = 128, full-dimension NeoX rotation.
 //
-// Mapping on sm_103a.  A 128-dim bf16 head row is 256 bytes = 16 lanes x one
-// 16-byte vector, so one warp covers two head rows per step: lanes 0-15 row
-// h, lanes 16-31 row h+1.  Lane l (of 16) holds dims 8l..8l+7; the NeoX
-// partner dims i +- 64 sit in lane l ^ 8 of the same half-warp, so one
-// 4-word shuffle of the raw bf16 values brings the partner in, and the
-// partner is then weighted with its own weight fragment.  The sum of squares
-// is a 4-step butterfly inside the half-warp.  A warp task is (token, chunk of
-// 2*STEPS consecutive Q/K head rows): the token's position and its 512-byte
-// cos/sin row are fetched once per task and reused for every row, and all
-// STEPS row loads are issued before any arithmetic so that each warp keeps
-// STEPS x 512 bytes in flight.  V columns are never addressed.
+// Mapping on sm_103a.  A 128-dim bf16 head row is 256 bytes; a half-warp
+// takes one row, so a warp covers two rows per step (lanes 0-15 row h, lanes
+// 16-31 row h+1).  Lane l (of 16) holds dims [4l, 4l+4) and their NeoX
+// partners [64+4l, 64+4l+4) -- two 8-byte loads that each form, across the
+// half-warp, one contiguous 128-byte segment -- so the rotation is local to
+// the lane: no shuffle brings the partner in, and each element of a pair is
+// weighted with its own dimension's weight before rotating.  The sum of
+// squares is a 4-step butterfly inside the half-warp.  A work item is
+// (token, chunk of consecutive Q/K head rows, at most 2*STEPS, chunks of a
+// token balanced in length): the token's position and the lane's 4 cosines
+// and 4 sines are fetched once per item and reused for every row, and all
+// row loads of an item are issued before any arithmetic.  V columns are
+// never addressed.  Two kernel shapes share the row arithmetic (so every
+// launch shape gives bit-identical results):
+//   * tiles:  one work item per warp, one-shot grid;
+//   * stream: persistent grid sized to the resident-CTA capacity, each warp
+//     taking grid-stride work items, weights loaded once per warp.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -37,87 +43,132 @@ struct QkParams {
   int num_tokens;
   int num_q;          // Hq
   int num_rows;       // Hq + Hk
-  int chunks;         // tasks per token
+  int chunks;         // work items per token
+  int steps;          // row pairs per chunk (<= the kernel's STEPS)
+  int items;          // num_tokens * chunks
   float eps;
 };
 
-template <int WARPS, int STEPS>
-__global__ void __launch_bounds__(WARPS * 32)
-qk_norm_rope_kernel(const QkParams p) {
-  const int lane = threadIdx.x & 31;
-  const int half = lane >> 4;
-  const int l16 = lane & 15;
-  const int task = blockIdx.x * WARPS + (threadIdx.x >> 5);
-  if (task >= p.num_tokens * p.chunks) return;  // whole warp leaves together
-  const int t = task / p.chunks;
-  const int first = (task - t * p.chunks) * (2 * STEPS) + half;
+// Weight fragments of this lane (dims [4l, 4l+4) and [64+4l, 64+4l+4), Q and
+// K), kept packed as bf16 and widened where they are used.
+struct QkWeights {
+  uint2 q_lo, q_hi, k_lo, k_hi;
+};
 
-  __nv_bfloat16* tok = p.qkv + (size_t)t * (size_t)p.row_elems;
+__device__ __forceinline__ void load_weights(const QkParams& p, int l16, QkWeights& w) {
+  const uint2* q = reinterpret_cast<const uint2*>(p.q_weight);
+  const uint2* k = reinterpret_cast<const uint2*>(p.k_weight);
+  w.q_lo = __ldg(q + l16);
+  w.q_hi = __ldg(q + 16 + l16);
+  w.k_lo = __ldg(k + l16);
+  w.k_hi = __ldg(k + 16 + l16);
+}
 
-  // 1. Issue every row load of this task first.
-  uint4 x[STEPS];
-#pragma unroll
-  for (int s = 0; s < STEPS; ++s) {
-    const int h = first + 2 * s;
-    x[s] = make_uint4(0u, 0u, 0u, 0u);
-    if (h < p.num_rows) x[s] = load_stream(tok + (size_t)h * kHeadDim + 8 * l16);
-  }
+__device__ __forceinline__ void unpack_bf16x4(const uint2& v, float* f) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xffff0000u);
+}
 
-  // 2. Token position, its cos/sin for this lane's 8 frequencies, weights.
+// The lane's 4 cosines and 4 sines of the token's row.
+__device__ __forceinline__ void load_cos_sin(const QkParams& p, int t, int l16, float4& c,
+                                             float4& s) {
   const int64_t pos = __ldg(p.positions + t);
-  const int f0 = 8 * (l16 & 7);  // frequency index of the lane's first dim
-  const float4* crow = reinterpret_cast<const float4*>(p.cos_sin + pos * kHeadDim + f0);
-  float c[8], sn[8];
-  {
-    const float4 c0 = __ldg(crow), c1 = __ldg(crow + 1);
-    const float4 s0 = __ldg(crow + kHalf / 4), s1 = __ldg(crow + kHalf / 4 + 1);
-    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
-    c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-    sn[0] = s0.x; sn[1] = s0.y; sn[2] = s0.z; sn[3] = s0.w;
-    sn[4] = s1.x; sn[5] = s1.y; sn[6] = s1.z; sn[7] = s1.w;
-  }
-  // out = n*cos - n_partner*sin for dims < 64, n*cos + n_partner*sin above.
-  const float sgn = (l16 < 8) ? -1.0f : 1.0f;
+  const float4* crow = reinterpret_cast<const float4*>(p.cos_sin + pos * kHeadDim);
+  c = __ldg(crow + l16);
+  s = __ldg(crow + kHalf / 4 + l16);
+}
+
+// Normalise + rotate one row fragment; all 32 lanes must call it together
+// (the sum of squares is reduced across the half-warp).
+__device__ __forceinline__ void row_math(uint2& lo, uint2& hi, bool is_q, const QkWeights& w,
+                                         const float4& c4, const float4& s4, float eps) {
+  float a[4], b[4];
+  unpack_bf16x4(lo, a);
+  unpack_bf16x4(hi, b);
+  float ss = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) sn[k] *= sgn;
+  for (int k = 0; k < 4; ++k) ss = fmaf(b[k], b[k], fmaf(a[k], a[k], ss));
+  ss = group_sum<16>(ss);
+  const float r = __frsqrt_rn(ss * (1.0f / kHeadDim) + eps);
+  float wa[4], wb[4];
+  unpack_bf16x4(is_q ? w.q_lo : w.k_lo, wa);
+  unpack_bf16x4(is_q ? w.q_hi : w.k_hi, wb);
+  const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+  const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+  float oa[4], ob[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float na = a[k] * r * wa[k];
+    const float nb = b[k] * r * wb[k];
+    oa[k] = fmaf(na, c[k], -nb * s[k]);
+    ob[k] = fmaf(nb, c[k], na * s[k]);
+  }
+  lo = make_uint2(pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]));
+  hi = make_uint2(pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]));
+}
 
-  float wq[8], wqp[8], wk[8], wkp[8];
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.q_weight) + l16), wq);
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.q_weight) + (l16 ^ 8)), wqp);
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.k_weight) + l16), wk);
-  unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.k_weight) + (l16 ^ 8)), wkp);
-
-  // 3. Normalise, rotate, store -- row by row.
+// One work item: token t, its chunk c of row pairs.  Lanes 0-15 take rows
+// first, first+2, ..; lanes 16-31 the rows after them.
+template <int STEPS>
+__device__ __forceinline__ void do_item(const QkParams& p, int item, int half, int l16,
+                                        const QkWeights& w) {
+  const int t = item / p.chunks;
+  const int c = item - t * p.chunks;
+  const int first = c * (2 * p.steps) + half;
+  const int last = min(p.num_rows, (c + 1) * (2 * p.steps));  // exclusive
+  __nv_bfloat16* tok = p.qkv + (size_t)t * (size_t)p.row_elems;
+  uint2 lo[STEPS], hi[STEPS];
 #pragma unroll
   for (int s = 0; s < STEPS; ++s) {
     const int h = first + 2 * s;
-    uint4 y;  // partner lane's raw values (dims +- 64)
-    y.x = __shfl_xor_sync(kFullMask, x[s].x, 8);
-    y.y = __shfl_xor_sync(kFullMask, x[s].y, 8);
-    y.z = __shfl_xor_sync(kFullMask, x[s].z, 8);
-    y.w = __shfl_xor_sync(kFullMask, x[s].w, 8);
-    float xf[8], yf[8];
-    unpack_bf16x8(x[s], xf);
-    unpack_bf16x8(y, yf);
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) ss = fmaf(xf[k], xf[k], ss);
-    ss = group_sum<16>(ss);
-    const float r = __frsqrt_rn(ss * (1.0f / kHeadDim) + p.eps);
-    const bool is_q = h < p.num_q;
-    float o[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float n = xf[k] * r * (is_q ? wq[k] : wk[k]);
-      const float np = yf[k] * r * (is_q ? wqp[k] : wkp[k]);
-      o[k] = fmaf(n, c[k], np * sn[k]);
+    lo[s] = hi[s] = make_uint2(0u, 0u);
+    if (h < last) {
+      const uint2* row = reinterpret_cast<const uint2*>(tok + (size_t)h * kHeadDim);
+      lo[s] = __ldcs(row + l16);
+      hi[s] = __ldcs(row + 16 + l16);
     }
-    if (h < p.num_rows) store_stream(tok + (size_t)h * kHeadDim + 8 * l16, pack_bf16x8(o));
+  }
+  float4 c4, s4;
+  load_cos_sin(p, t, l16, c4, s4);
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    if (first - half + 2 * s >= last) break;  // warp-uniform: no row left in the chunk
+    const int h = first + 2 * s;
+    row_math(lo[s], hi[s], h < p.num_q, w, c4, s4, p.eps);
+    if (h < last) {
+      uint2* row = reinterpret_cast<uint2*>(tok + (size_t)h * kHeadDim);
+      __stcs(row + l16, lo[s]);
+      __stcs(row + 16 + l16, hi[s]);
+    }
   }
 }
 
-template <int WARPS, int STEPS>
-cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
+template <int WARPS, int STEPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+qk_tiles_kernel(const QkParams p) {
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  if (item >= p.items) return;  // whole warp leaves together
+  QkWeights w;
+  load_weights(p, lane & 15, w);
+  do_item<STEPS>(p, item, lane >> 4, lane & 15, w);
+}
+
+template <int WARPS, int STEPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+qk_stream_kernel(const QkParams p) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  if (gw >= p.items) return;
+  QkWeights w;
+  load_weights(p, lane & 15, w);
+  for (int item = gw; item < p.items; item += nw) do_item<STEPS>(p, item, lane >> 4, lane & 15, w);
+}
+
+QkParams make_params(const QkArgs& a, int steps) {
   QkParams p;
   p.qkv = static_cast<__nv_bfloat16*>(a.qkv);
   p.q_weight = static_cast<const __nv_bfloat16*>(a.q_weight);
@@ -128,27 +179,54 @@ cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
   p.row_elems = (int64_t)(p.num_rows + a.num_heads_v) * kHeadDim;
   p.num_tokens = a.num_tokens;
   p.num_q = a.num_heads_q;
-  p.chunks = (p.num_rows + 2 * STEPS - 1) / (2 * STEPS);
+  // Balanced chunks: as few as STEPS allows, then as short as possible.
+  const int pairs = (p.num_rows + 1) / 2;
+  p.chunks = (pairs + steps - 1) / steps;
+  p.steps = (pairs + p.chunks - 1) / p.chunks;
+  p.items = p.num_tokens * p.chunks;
   p.eps = a.eps;
-  const int64_t tasks = (int64_t)p.num_tokens * p.chunks;
-  const unsigned grid = (unsigned)((tasks + WARPS - 1) / WARPS);
-  qk_norm_rope_kernel<WARPS, STEPS><<<grid, WARPS * 32, 0, stream>>>(p);
+  return p;
+}
+
+template <int WARPS, int STEPS, int MINB>
+cudaError_t launch_tiles(const QkArgs& a, cudaStream_t stream) {
+  const QkParams p = make_params(a, STEPS);
+  const unsigned grid = (unsigned)((p.items + WARPS - 1) / WARPS);
+  qk_tiles_kernel<WARPS, STEPS, MINB><<<grid, WARPS * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int WARPS, int STEPS, int MINB>
+cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
+  const QkParams p = make_params(a, STEPS);
+  int per_sm = 0;
+  cudaError_t e = resident_ctas(qk_stream_kernel<WARPS, STEPS, MINB>, WARPS * 32, &per_sm);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (int64_t)per_sm * device_sm_count();
+  const int64_t need = (p.items + WARPS - 1) / WARPS;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  qk_stream_kernel<WARPS, STEPS, MINB><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// Rows (Q+K heads x tokens) below which the one-row-pair-per-warp launch is
-// used: it spreads a decode-sized batch over the most SMs.
-constexpr int64_t kQkSmallRows = 152 * 4 * 2;
+const LaunchConfig kQkConfigs[] = {
+    {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"},
+    {"tiles<8w,4step>"}, {"stream<8w,4step>"},
+};
+const int kQkNumConfigs = sizeof(kQkConfigs) / sizeof(kQkConfigs[0]);
 
-int qk_path(int64_t num_tokens, int num_rows_per_token) {
-  return num_tokens * (int64_t)num_rows_per_token < kQkSmallRows ? 0 : 1;
-}
-
-cudaError_t launch_qk_norm_rope(const QkArgs& a, int path, cudaStream_t stream) {
-  if (path == 0) return launch<4, 1>(a, stream);
-  return launch<8, 4>(a, stream);
+cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream) {
+  switch (config) {
+    case 0: return launch_tiles<4, 1, 1>(a, stream);
+    case 1: return launch_tiles<8, 2, 1>(a, stream);
+    case 2: return launch_tiles<4, 4, 1>(a, stream);
+    case 3: return launch_tiles<8, 4, 1>(a, stream);
+    case 4: return launch_stream<8, 4, 1>(a, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace kvq

@@ -131,5 +131,16 @@ def with_threshold(value):
     return _Ctx()
 
 
+def with_config(op, config_id):
+    """Context manager forcing launch configuration ``config_id`` of ``op``."""
+    class _Ctx:
+        def __enter__(self):
+            self.old = kvq.set_config(op, config_id)
+
+        def __exit__(self, *exc):
+            kvq.set_config(op, self.old)
+    return _Ctx()
+
+
 SMALL_PATH = 1 << 40   # threshold above any program count: small-batch launch
 TILED_PATH = 0         # every call takes the token-tiled launch

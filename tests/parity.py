@@ -91,8 +91,9 @@ class CacheReport:
     def check(self, what=""):
         assert self.exp_mismatch_bad == 0, f"{what}: {self.exp_mismatch_bad} exponent bytes differ"
         assert self.codes_far == 0, f"{what}: {self.codes_far} e4m3 codes more than one code apart"
-        frac = self.codes_exact / max(self.codes, 1)
-        assert frac >= CODE_EXACT_MIN, f"{what}: only {frac:.6f} of e4m3 codes bit-exact"
+        if self.codes:
+            frac = self.codes_exact / self.codes
+            assert frac >= CODE_EXACT_MIN, f"{what}: only {frac:.6f} of e4m3 codes bit-exact"
         self.rope.check(what + " (rotary bf16 in cache)")
 
 

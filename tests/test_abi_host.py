@@ -138,3 +138,26 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(kvq, "LIB_PATH", str(tmp_path / "libkvq.so"))
     with pytest.raises(kvq.KvqError):
         kvq.lib()
+
+
+def test_launch_config_table(L):
+    for op in ("qk", "dsv4"):
+        names = kvq.configs(op)
+        assert len(names) >= 2 and len(set(names)) == len(names)
+        assert getattr(L, f"kvq_{op}_config_name")(len(names)) is None
+        assert getattr(L, f"kvq_{op}_config_name")(-1) is None
+        prev = kvq.set_config(op, len(names) - 1)
+        try:
+            assert kvq.set_config(op, 0) == len(names) - 1
+            with pytest.raises(ValueError):
+                kvq.set_config(op, len(names))
+            assert kvq.set_config(op, 0) == 0   # unchanged by the rejected id
+        finally:
+            kvq.set_config(op, prev)
+    kvq.set_config("dsv4", 3)
+    try:
+        assert kvq.dsv4_config_for(131072, 128) == 3 and kvq.dsv4_config_for(1, 1) == 3
+    finally:
+        kvq.set_config("dsv4", -1)
+    assert kvq.dsv4_config_for(1, 1) in range(len(kvq.configs("dsv4")))
+    assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))

@@ -5,7 +5,8 @@ import torch
 
 import kv_quant_cache_gb300 as kvq
 import workloads as wl
-from gpu_cases import SMALL_PATH, TILED_PATH, dsv4_parity, run_dsv4, to_device, with_threshold
+from gpu_cases import (SMALL_PATH, TILED_PATH, dsv4_parity, run_dsv4, to_device, with_config,
+                       with_threshold)
 
 pytestmark = pytest.mark.gpu
 
@@ -136,3 +137,18 @@ def test_repeat_calls_are_deterministic(cuda_device):
     run_dsv4(d2)
     torch.cuda.synchronize()
     assert torch.equal(d["q"], d2["q"]) and torch.equal(d["kv_cache"], d2["kv_cache"])
+
+
+DSV4_CONFIGS = list(range(5))
+
+
+@pytest.mark.parametrize("config", DSV4_CONFIGS)
+@pytest.mark.parametrize("shape", [(1, 1), (17, 3), (777, 5), (2048, 64)])
+def test_every_launch_config(cuda_device, config, shape):
+    """Each launch shape of the table against the oracle (forced)."""
+    assert len(kvq.configs("dsv4")) == len(DSV4_CONFIGS)
+    T, H = shape
+    d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 16), block_size=16,
+                     slots="distinct_skip2", seed=300 + config, device=cuda_device)
+    with with_config("dsv4", config):
+        dsv4_parity(d)

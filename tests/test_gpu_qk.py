@@ -5,7 +5,7 @@ import torch
 
 import kv_quant_cache_gb300 as kvq
 import workloads as wl
-from gpu_cases import qk_parity, to_device
+from gpu_cases import qk_parity, to_device, with_config
 
 pytestmark = pytest.mark.gpu
 
@@ -82,3 +82,18 @@ def test_runs_on_a_side_stream(cuda_device):
     s.synchronize()
     qk_parity(ref)  # the same inputs through the default stream
     assert torch.equal(d["qkv"], ref["qkv"])
+
+
+QK_CONFIGS = list(range(5))
+
+
+@pytest.mark.parametrize("config", QK_CONFIGS)
+@pytest.mark.parametrize("shape", [(1, 16, 8, 8), (777, 5, 3, 2), (300, 32, 8, 8), (64, 1, 0, 1)])
+def test_every_launch_config(cuda_device, config, shape):
+    """Each launch shape of the table against the oracle (forced), on ragged
+    token counts and head counts that leave partial chunks."""
+    assert len(kvq.configs("qk")) == len(QK_CONFIGS)
+    T, Hq, Hk, Hv = shape
+    d = wl.make_qk(T, Hq, Hk, Hv, theta=1e6, max_pos=131072, seed=31 + config, device=cuda_device)
+    with with_config("qk", config):
+        qk_parity(d)
