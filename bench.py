@@ -234,44 +234,68 @@ def time_device(kvq, qk, ds, steps, warmup, world, device):
     return total_ms, qk_ms, ds_ms
 
 
-def time_e2e(kvq, qk, ds, steps, device):
+def time_e2e(kvq, qk, ds, steps, device, chunks=8):
     """Same step with host buffers: pinned inputs copied in, the kernels, the
-    results (q, qkv, cache) copied out, every step inside the timed region."""
-    h = {
-        "qkv": qk["qkv"].cpu().pin_memory(), "qk_pos": qk["positions"].cpu().pin_memory(),
-        "q": ds["q"].cpu().pin_memory(), "kv": ds["kv"].cpu().pin_memory(),
-        "ds_pos": ds["positions"].cpu().pin_memory(), "slot": ds["slot_mapping"].cpu().pin_memory(),
-    }
+    results (qkv, q, cache) copied out, every step inside the timed region.
+    Tokens are independent, so the step is cut into `chunks` token ranges and
+    three streams overlap the host->device copy of chunk i+1, the two kernels
+    on chunk i and the device->host copy of chunk i-1."""
+    h = {"qkv": qk["qkv"].cpu().pin_memory(), "qk_pos": qk["positions"].cpu().pin_memory(),
+         "q": ds["q"].cpu().pin_memory(), "kv": ds["kv"].cpu().pin_memory(),
+         "ds_pos": ds["positions"].cpu().pin_memory(),
+         "slot": ds["slot_mapping"].cpu().pin_memory()}
     out = {"qkv": torch.empty_like(h["qkv"]).pin_memory(), "q": torch.empty_like(h["q"]).pin_memory(),
            "cache": torch.empty(ds["kv_cache"].shape, dtype=torch.uint8).pin_memory()}
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in out.values())
-    stream = torch.cuda.Stream(device)
+    T = qk["qkv"].shape[0]
+    bounds = [(i * T // chunks, (i + 1) * T // chunks) for i in range(chunks)]
+    s_in, s_run, s_out = (torch.cuda.Stream(device) for _ in range(3))
 
     def one():
-        qk["qkv"].copy_(h["qkv"], non_blocking=True)
-        qk["positions"].copy_(h["qk_pos"], non_blocking=True)
-        ds["q"].copy_(h["q"], non_blocking=True)
-        ds["kv"].copy_(h["kv"], non_blocking=True)
-        ds["positions"].copy_(h["ds_pos"], non_blocking=True)
-        ds["slot_mapping"].copy_(h["slot"], non_blocking=True)
-        launch_qk(kvq, qk, stream)
-        launch_dsv4(kvq, ds, stream)
-        out["qkv"].copy_(qk["qkv"], non_blocking=True)
-        out["q"].copy_(ds["q"], non_blocking=True)
-        out["cache"].copy_(ds["kv_cache"], non_blocking=True)
+        ev_k = []
+        for a, b in bounds:
+            with torch.cuda.stream(s_in):
+                qk["qkv"][a:b].copy_(h["qkv"][a:b], non_blocking=True)
+                qk["positions"][a:b].copy_(h["qk_pos"][a:b], non_blocking=True)
+                ds["q"][a:b].copy_(h["q"][a:b], non_blocking=True)
+                ds["kv"][a:b].copy_(h["kv"][a:b], non_blocking=True)
+                ds["positions"][a:b].copy_(h["ds_pos"][a:b], non_blocking=True)
+                ds["slot_mapping"][a:b].copy_(h["slot"][a:b], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_run.wait_event(ev_in)
+            kvq.fused_qk_norm_rope(qk["qkv"][a:b], qk["Hq"], qk["Hk"], qk["Hv"], qk["D"], qk["eps"],
+                                   qk["q_weight"], qk["k_weight"], qk["cos_sin"], True,
+                                   qk["positions"][a:b], stream=s_run)
+            kvq.dsv4_qnorm_rope_kv_rope_quant_insert(
+                ds["q"][a:b], ds["kv"][a:b], ds["eps"], ds["q_weight"], ds["kv_weight"],
+                ds["cos_sin"], ds["positions"][a:b], ds["slot_mapping"][a:b], ds["kv_cache"],
+                stream=s_run)
+            ev = torch.cuda.Event()
+            ev.record(s_run)
+            ev_k.append(ev)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                out["qkv"][a:b].copy_(qk["qkv"][a:b], non_blocking=True)
+                out["q"][a:b].copy_(ds["q"][a:b], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            out["cache"].copy_(ds["kv_cache"], non_blocking=True)
+        # the next step's inputs may only overwrite a chunk once its results are out
+        ev_done = torch.cuda.Event()
+        ev_done.record(s_out)
+        s_in.wait_event(ev_done)
 
-    with torch.cuda.stream(stream):
+    one()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    for _ in range(steps):
         one()
-        stream.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(steps):
-            one()
-        end.record(stream)
-    stream.synchronize()
-    return start.elapsed_time(end) / steps, h2d, d2h
+    end.record(s_out)
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(end) / steps, h2d, d2h, chunks
 
 
 def host_step_inputs(qk, ds):
@@ -334,11 +358,12 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
-        e2e_ms, h2d, d2h = time_e2e(kvq, qk, ds, e2e_steps, device)
+        e2e_ms, h2d, d2h, n_chunks = time_e2e(kvq, qk, ds, e2e_steps, device)
         e2e_ms = max_over_ranks(e2e_ms, world, device)
         e2e = {"value": round(world * (b_qk + b_ds) / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "steps": e2e_steps}
+               "steps": e2e_steps, "pipeline": f"{n_chunks} token chunks, copy-in / kernels / "
+                                                 "copy-out on three streams"}
     cpu = None
     if host_inputs is not None:
         v, cores, dt = cpu_baseline(qk, ds, *host_inputs)
@@ -363,6 +388,8 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": b_ds},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+        "dispatch": {"qk": kvq.configs("qk")[kvq.qk_config_for(32768, 32, 8)],
+                     "dsv4": kvq.configs("dsv4")[kvq.dsv4_config_for(32768, 64)]},
     }
     if args.sweep and rank == 0:
         sweep(kvq, device)

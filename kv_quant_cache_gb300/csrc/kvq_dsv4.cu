@@ -22,7 +22,8 @@
 //   * Cache entry: chunk-0 codes are 32 x 8 contiguous bytes, chunk-1 codes
 //     and the rotary bf16 values the next 320 bytes, and lane 0 writes the
 //     seven exponent bytes plus the pad as one 8-byte store.  slot * 584 is a
-//     multiple of 8, so every store is naturally aligned.
+//     multiple of 8, so every store is naturally aligned; all are streaming
+//     (evict-first) stores.
 // No warp mixes the light Q work with the heavier KV work (the pages'
 // slot-type-uniform programs).  Two kernel shapes:
 //   * tiles:  one-shot grid; the first CTAs take KV vectors (one token per
@@ -156,6 +157,15 @@ __device__ __forceinline__ void q_row(const Dsv4Params& p, int row, const RowReg
   store_stream(dst + 256 + 8 * lane, pack_bf16x8(x + 8));
 }
 
+// Entry stores are streaming (evict-first), like the q stores.  Measured on
+// GB300: with default write-back stores the entries of a large batch linger
+// in L2 and cost the q stream up to 10% when the cache exceeds L2 (153 MB
+// cache, 131072 tokens); evict-first stores bring the kernel within 2% of
+// the same launch without any cache write.
+__device__ __forceinline__ void store8(uint8_t* dst, uint2 v) {
+  __stcs(reinterpret_cast<uint2*>(dst), v);
+}
+
 __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, const RowRegs& r,
                                          const Weights& w, int lane) {
   float x[16];
@@ -181,17 +191,17 @@ __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, cons
   const uint32_t g6 = __shfl_sync(kFullMask, e1, 16);
   if (slot < 0) return;  // warp-uniform: the token has no cache slot
   uint8_t* ent = p.kv_cache + slot * kEntry;
-  *reinterpret_cast<uint2*>(ent + 8 * lane) = codes0;
+  store8(ent + 8 * lane, codes0);
   if (lane < kRopeLane) {
-    *reinterpret_cast<uint2*>(ent + 256 + 8 * lane) = codes1;
+    store8(ent + 256 + 8 * lane, codes1);
   } else {
-    uint2* dst = reinterpret_cast<uint2*>(ent + kRopeAt + 16 * (lane - kRopeLane));
-    dst[0] = make_uint2(rope.x, rope.y);
-    dst[1] = make_uint2(rope.z, rope.w);
+    uint8_t* dst = ent + kRopeAt + 16 * (lane - kRopeLane);
+    store8(dst, make_uint2(rope.x, rope.y));
+    store8(dst + 8, make_uint2(rope.z, rope.w));
   }
   if (lane == 0) {
-    *reinterpret_cast<uint2*>(ent + kScaleAt) =
-        make_uint2(g0 | (g1 << 8) | (g2 << 16) | (g3 << 24), g4 | (g5 << 8) | (g6 << 16));
+    store8(ent + kScaleAt, make_uint2(g0 | (g1 << 8) | (g2 << 16) | (g3 << 24),
+                                                   g4 | (g5 << 8) | (g6 << 16)));
   }
 }
 
@@ -227,28 +237,20 @@ dsv4_tiles_kernel(const Dsv4Params p) {
 
 // ---- stream: persistent grid, two-deep register pipeline ------------------
 
-template <int WARPS, int MINB>
-__global__ void __launch_bounds__(WARPS * 32, MINB)
-dsv4_stream_kernel(const Dsv4Params p) {
-  const int lane = threadIdx.x & 31;
-  const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
-  const int nw = (int)gridDim.x * WARPS;
-  Weights w;
-
-  // KV vectors first: each warp's share is small and the heavier per-token
-  // work then overlaps with other warps' q streaming.
-  if (gw < p.num_tokens) {
-    w = load_weights(p.kv_weight, lane);
-    for (int t = gw; t < p.num_tokens; t += nw) {
-      RowRegs r;
-      load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
-      kv_token(p, __ldg(p.slot_mapping + t), r, w, lane);
-    }
+__device__ __forceinline__ void stream_kv(const Dsv4Params& p, int gw, int nw, int lane) {
+  if (gw >= p.num_tokens) return;
+  const Weights w = load_weights(p.kv_weight, lane);
+  for (int t = gw; t < p.num_tokens; t += nw) {
+    RowRegs r;
+    load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
+    kv_token(p, __ldg(p.slot_mapping + t), r, w, lane);
   }
+}
 
+__device__ __forceinline__ void stream_q(const Dsv4Params& p, int gw, int nw, int lane) {
   int row = gw;
   if (row >= p.q_rows) return;
-  w = load_weights(p.q_weight, lane);
+  const Weights w = load_weights(p.q_weight, lane);
   RowRegs r0, r1;
   load_row(p, p.q + (size_t)row * kDim, row / p.num_heads, lane, r0);
   while (true) {
@@ -263,6 +265,18 @@ dsv4_stream_kernel(const Dsv4Params p) {
     if (next >= p.q_rows) break;
     row = next;
   }
+}
+
+// KV vectors first: each warp's share is small, and running them last was
+// measured no faster.
+template <int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+dsv4_stream_kernel(const Dsv4Params p) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = (int)gridDim.x * WARPS;
+  stream_kv(p, gw, nw, lane);
+  stream_q(p, gw, nw, lane);
 }
 
 Dsv4Params make_params(const Dsv4Args& a) {
