@@ -31,9 +31,16 @@
  *       entry; this library defines them as listed below.
  *
  * General contract (both operators)
- *   - All pointers are DEVICE pointers of the current CUDA device and are
- *     owned by the caller.  The library allocates no memory, keeps no
- *     per-call state, and never synchronises the stream.
+ *   - Every pointer must be dereferenceable by the current CUDA device at
+ *     the address given: device memory, or host memory mapped into the
+ *     device's address space at the same address (pinned with cudaHostAlloc
+ *     or cudaHostRegister on a unified-addressing system).  On an
+ *     NVLink-C2C coherent system (Grace-Blackwell) the kernels then read and
+ *     write such host buffers directly over the interconnect, one pass, with
+ *     no staging copy -- V of the packed QKV tensor never crosses it.  The
+ *     library does not check which kind a pointer is.
+ *   - All buffers are owned by the caller.  The library allocates no memory,
+ *     keeps no per-call state, and never synchronises the stream.
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  A KVQ_OK
  *     return means "validated and enqueued"; kernel faults surface on the
  *     stream like any other kernel's.

@@ -1,8 +1,9 @@
 """GB300 (sm_103a) attention-prologue kernels -- Python binding of include/kvq.h.
 
-This module only marshals arguments: it checks that tensors are CUDA tensors of
-the expected dtype and layout, takes their device pointers and the current
-stream, and calls the C ABI in ``libkvq.so``.  Every step of the computation
+This module only marshals arguments: it checks that tensors are CUDA tensors
+(or pinned host tensors, which the kernels then access in place over the
+host interconnect) of the expected dtype and layout, takes their addresses
+and the current stream, and calls the C ABI in ``libkvq.so``.  Every step of the computation
 runs in the CUDA kernels; there is no CPU or PyTorch fallback.  If the library
 has not been built, importing works but every call raises ``KvqError``.
 
@@ -99,8 +100,11 @@ def _check(status: int, fn: str) -> None:
 
 
 def _cuda(t: torch.Tensor, dtype, name: str) -> int:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name}: expected a CUDA tensor")
+    """Address of a CUDA tensor, or of a pinned host tensor (mapped into the
+    device's address space at the same address under unified addressing)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu"
+                                                             and t.is_pinned())):
+        raise ValueError(f"{name}: expected a CUDA tensor or a pinned host tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -110,7 +114,7 @@ def _cuda(t: torch.Tensor, dtype, name: str) -> int:
 
 def _stream(stream, device) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream(device)
+        stream = torch.cuda.current_stream(device if device.type == "cuda" else None)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
