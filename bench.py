@@ -74,10 +74,14 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+DSV4_KERNEL_SOURCES = ("kvq_dsv4.cu", "kvq_device.cuh", "kvq_launch.h")
+
+
+def kernel_source_hash(files=DSV4_KERNEL_SOURCES):
+    """Hash of the sources one kernel is built from (default: the DSV4 kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_quant_cache_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -24,6 +24,9 @@
 //   * tiles:  one work item per warp, one-shot grid;
 //   * stream: persistent grid sized to the resident-CTA capacity, each warp
 //     taking grid-stride work items, weights loaded once per warp.
+// (A persistent variant that keeps the next item's loads in flight, the
+// shape that wins for the DSV4 operator, measured 45-71 % here and is not
+// kept: at 74-86 registers it holds too few warps.)
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -109,40 +112,70 @@ __device__ __forceinline__ void row_math(uint2& lo, uint2& hi, bool is_q, const 
   hi = make_uint2(pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]));
 }
 
-// One work item: token t, its chunk c of row pairs.  Lanes 0-15 take rows
+// One work item's rows as held by a lane: STEPS row fragments plus the
+// token's cosines and sines for the lane's 4 frequencies.
+template <int STEPS>
+struct ItemRegs {
+  uint2 lo[STEPS], hi[STEPS];
+  float4 c, s;
+};
+
+// Work item `item` = (token t, chunk c of row pairs).  Lanes 0-15 take rows
 // first, first+2, ..; lanes 16-31 the rows after them.
+struct ItemPos {
+  int t, first, last;  // token, this lane's first row, end of the chunk
+};
+
+__device__ __forceinline__ ItemPos item_pos(const QkParams& p, int item, int half) {
+  ItemPos ip;
+  ip.t = item / p.chunks;
+  const int c = item - ip.t * p.chunks;
+  ip.first = c * (2 * p.steps) + half;
+  ip.last = min(p.num_rows, (c + 1) * (2 * p.steps));
+  return ip;
+}
+
+template <int STEPS>
+__device__ __forceinline__ void load_item(const QkParams& p, const ItemPos& ip, int l16,
+                                          ItemRegs<STEPS>& r) {
+  const __nv_bfloat16* tok = p.qkv + (size_t)ip.t * (size_t)p.row_elems;
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const int h = ip.first + 2 * s;
+    r.lo[s] = r.hi[s] = make_uint2(0u, 0u);
+    if (h < ip.last) {
+      const uint2* row = reinterpret_cast<const uint2*>(tok + (size_t)h * kHeadDim);
+      r.lo[s] = __ldcs(row + l16);
+      r.hi[s] = __ldcs(row + 16 + l16);
+    }
+  }
+  load_cos_sin(p, ip.t, l16, r.c, r.s);
+}
+
+template <int STEPS>
+__device__ __forceinline__ void compute_item(const QkParams& p, const ItemPos& ip, int half,
+                                             int l16, const QkWeights& w, ItemRegs<STEPS>& r) {
+  __nv_bfloat16* tok = p.qkv + (size_t)ip.t * (size_t)p.row_elems;
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    if (ip.first - half + 2 * s >= ip.last) break;  // warp-uniform: no row left in the chunk
+    const int h = ip.first + 2 * s;
+    row_math(r.lo[s], r.hi[s], h < p.num_q, w, r.c, r.s, p.eps);
+    if (h < ip.last) {
+      uint2* row = reinterpret_cast<uint2*>(tok + (size_t)h * kHeadDim);
+      __stcs(row + l16, r.lo[s]);
+      __stcs(row + 16 + l16, r.hi[s]);
+    }
+  }
+}
+
 template <int STEPS>
 __device__ __forceinline__ void do_item(const QkParams& p, int item, int half, int l16,
                                         const QkWeights& w) {
-  const int t = item / p.chunks;
-  const int c = item - t * p.chunks;
-  const int first = c * (2 * p.steps) + half;
-  const int last = min(p.num_rows, (c + 1) * (2 * p.steps));  // exclusive
-  __nv_bfloat16* tok = p.qkv + (size_t)t * (size_t)p.row_elems;
-  uint2 lo[STEPS], hi[STEPS];
-#pragma unroll
-  for (int s = 0; s < STEPS; ++s) {
-    const int h = first + 2 * s;
-    lo[s] = hi[s] = make_uint2(0u, 0u);
-    if (h < last) {
-      const uint2* row = reinterpret_cast<const uint2*>(tok + (size_t)h * kHeadDim);
-      lo[s] = __ldcs(row + l16);
-      hi[s] = __ldcs(row + 16 + l16);
-    }
-  }
-  float4 c4, s4;
-  load_cos_sin(p, t, l16, c4, s4);
-#pragma unroll
-  for (int s = 0; s < STEPS; ++s) {
-    if (first - half + 2 * s >= last) break;  // warp-uniform: no row left in the chunk
-    const int h = first + 2 * s;
-    row_math(lo[s], hi[s], h < p.num_q, w, c4, s4, p.eps);
-    if (h < last) {
-      uint2* row = reinterpret_cast<uint2*>(tok + (size_t)h * kHeadDim);
-      __stcs(row + l16, lo[s]);
-      __stcs(row + 16 + l16, hi[s]);
-    }
-  }
+  const ItemPos ip = item_pos(p, item, half);
+  ItemRegs<STEPS> r;
+  load_item<STEPS>(p, ip, l16, r);
+  compute_item<STEPS>(p, ip, half, l16, w, r);
 }
 
 template <int WARPS, int STEPS, int MINB>
@@ -196,25 +229,30 @@ cudaError_t launch_tiles(const QkArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int WARPS, int STEPS, int MINB>
-cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
-  const QkParams p = make_params(a, STEPS);
+template <typename Kernel>
+cudaError_t launch_persistent(Kernel kernel, const QkParams& p, int warps, cudaStream_t stream) {
   int per_sm = 0;
-  cudaError_t e = resident_ctas(qk_stream_kernel<WARPS, STEPS, MINB>, WARPS * 32, &per_sm);
+  cudaError_t e = resident_ctas(kernel, warps * 32, &per_sm);
   if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)per_sm * device_sm_count();
-  const int64_t need = (p.items + WARPS - 1) / WARPS;
+  const int64_t need = (p.items + warps - 1) / warps;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  qk_stream_kernel<WARPS, STEPS, MINB><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
+  kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int WARPS, int STEPS, int MINB>
+cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
+  return launch_persistent(qk_stream_kernel<WARPS, STEPS, MINB>, make_params(a, STEPS), WARPS,
+                           stream);
 }
 
 }  // namespace
 
 const LaunchConfig kQkConfigs[] = {
-    {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"},
-    {"tiles<8w,4step>"}, {"stream<8w,4step>"},
+    {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"}, {"tiles<8w,4step>"},
+    {"stream<8w,4step>"},
 };
 const int kQkNumConfigs = sizeof(kQkConfigs) / sizeof(kQkConfigs[0]);
 
