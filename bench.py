@@ -47,10 +47,11 @@ PROFILES = os.path.join(ROOT, "profiles")
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
-def qk_bytes(T, Hq, Hk, D=128):
-    """Q and K heads read and written once (bf16), one cos/sin row (fp32) and
-    one position (int64) per token, the two weight vectors once."""
-    return T * ((Hq + Hk) * D * 2 * 2 + D * 4 + 8) + 2 * D * 2
+def qk_bytes(T, Hq, Hk, D=128, rot=None):
+    """Q and K heads read and written once (bf16), one cos/sin row of `rot`
+    floats and one position (int64) per token, the two weight vectors once."""
+    rot = D if rot is None else rot
+    return T * ((Hq + Hk) * D * 2 * 2 + rot * 4 + 8) + 2 * D * 2
 
 
 def dsv4_bytes(T, H, mapped):
@@ -552,6 +553,28 @@ def sweep(kvq, device):
     for w in (wl.QK_SMALL, wl.QK_LARGE):
         d = wl.make_qk_workload(w, device=device)
         run_configs("qk", w.name, qk_bytes(w.T, w.Hq, w.Hk), lambda: launch_qk(kvq, d, stream), 30)
+        del d
+    # the general QK kernel (head_dim 64/256, GPT-J pairs, partial rotation)
+    for (T, hq, hk, hv, D, rot, neox) in ((32768, 32, 8, 8, 64, 64, True),
+                                          (32768, 32, 8, 8, 128, 64, False),
+                                          (32768, 32, 8, 8, 128, 128, False),
+                                          (16384, 32, 8, 8, 256, 256, True),
+                                          (16384, 32, 8, 8, 256, 64, False),
+                                          (17, 16, 8, 8, 256, 256, True)):
+        d = wl.make_qk(T, hq, hk, hv, D=D, theta=1e6, max_pos=131072, seed=D + rot,
+                       device=device, rotary_dim=rot, is_neox=neox)
+        nb = qk_bytes(T, hq, hk, D, rot)
+        small = nb < 256 * 2**20
+
+        def fn():
+            kvq.fused_qk_norm_rope(d["qkv"], hq, hk, hv, D, d["eps"], d["q_weight"],
+                                   d["k_weight"], d["cos_sin"], neox, d["positions"],
+                                   stream=stream, rotary_dim=rot)
+        med, _ = _time_launch(fn, 30, stream, flush if small else None)
+        emit({"sweep": f"qk_T{T}_{hq}-{hk}-{hv}_D{D}_rot{rot}_{'neox' if neox else 'gptj'}",
+              "config": "general", "bytes": nb, "us_median": round(med * 1e3, 2),
+              "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
+              "l2_flush": small})
         del d
     for w in [wl.DSV4_DECODE, wl.DSV4_LARGE, *wl.DSV4_SWEEP]:
         d = wl.make_dsv4_workload(w, device=device)

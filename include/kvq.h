@@ -71,37 +71,15 @@ typedef enum kvq_status {
   KVQ_OK = 0,
   KVQ_ERR_NULL = 1,        /* a required pointer is NULL */
   KVQ_ERR_SHAPE = 2,       /* negative or too-large count, bad block_size */
-  KVQ_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
+  KVQ_ERR_UNSUPPORTED = 3, /* head_dim / rotary_dim / is_neox outside the set above */
   KVQ_ERR_ALIGN = 4,       /* a pointer is not aligned as required below */
   KVQ_ERR_CUDA = 5,        /* the kernel launch itself failed */
   KVQ_ERR_VALUE = 6        /* eps negative or not finite */
 } kvq_status;
 
 /*
- * fused_qk_norm_rope -- in place on qkv.
- *
- *   qkv            bf16 [num_tokens, (Hq + Hk + Hv) * head_dim], row-major,
- *                  contiguous, 16-byte aligned.  Per token: Hq query heads,
- *                  then Hk key heads, then Hv value heads, head_dim each.
- *                  Q and K heads are replaced by their normalised, rotated
- *                  values; V heads are not accessed.
- *   num_tokens     T >= 0 (T * (Hq + Hk) must stay below 2^31).
- *   num_heads_q/k/v  >= 0 each.
- *   head_dim       must be 128 (else KVQ_ERR_UNSUPPORTED).
- *   eps            added to the mean square inside the square root; finite,
- *                  >= 0.
- *   q_weight, k_weight  bf16 [head_dim] RMSNorm weights, 16-byte aligned.
- *   cos_sin_cache  fp32 [max_pos, head_dim]; row p holds cos(p * f_i) for
- *                  i < head_dim/2 followed by sin(p * f_i); 16-byte aligned.
- *   is_neox        must be 1: dim i pairs with dim i + head_dim/2 (else
- *                  KVQ_ERR_UNSUPPORTED).
- *   positions      int64 [num_tokens], 8-byte aligned, each < max_pos.
- *
- * Per head row x (fp32 arithmetic, one bf16 round-to-nearest-even at the end):
- *   r = 1 / sqrt(sum(x^2) / head_dim + eps);  n_i = x_i * r * w_i
- *   out_i       = n_i * cos_i - n_{i+64} * sin_i        (i < 64)
- *   out_{i+64}  = n_{i+64} * cos_i + n_i * sin_i
- * so the partner enters with its own dimension's weight.
+ * fused_qk_norm_rope -- in place on qkv; full-dimension rotation
+ * (rotary_dim = head_dim).  Same as fused_qk_norm_rope_ex below.
  */
 kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
                               int num_heads_k, int num_heads_v, int head_dim,
@@ -109,6 +87,47 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
                               const void* k_weight, const float* cos_sin_cache,
                               int is_neox, const int64_t* positions,
                               kvq_stream_t stream);
+
+/*
+ * fused_qk_norm_rope_ex -- in place on qkv, with a rotary width.
+ *
+ *   qkv            bf16 [num_tokens, (Hq + Hk + Hv) * head_dim], row-major,
+ *                  contiguous, 16-byte aligned.  Per token: Hq query heads,
+ *                  then Hk key heads, then Hv value heads, head_dim each.
+ *                  Q and K heads are replaced by their normalised, rotated
+ *                  values; V heads are not accessed.
+ *   num_tokens     T >= 0 (T * (Hq + Hk + 1) must stay below 2^31).
+ *   num_heads_q/k/v  >= 0 each.
+ *   head_dim       64, 128 or 256 (else KVQ_ERR_UNSUPPORTED).
+ *   eps            added to the mean square inside the square root; finite,
+ *                  >= 0.
+ *   q_weight, k_weight  bf16 [head_dim] RMSNorm weights, 16-byte aligned.
+ *   cos_sin_cache  fp32 [max_pos, rotary_dim]; row p holds cos(p * f_i) for
+ *                  i < rotary_dim/2 followed by sin(p * f_i); 16-byte aligned.
+ *   rotary_dim     rotated width: a multiple of 16 in [16, head_dim] (else
+ *                  KVQ_ERR_UNSUPPORTED); the first rotary_dim dims of each
+ *                  head rotate, the rest are normalised only.
+ *   is_neox        1: dim i pairs with dim i + rotary_dim/2 (NeoX);
+ *                  0: dim 2i pairs with dim 2i+1 (GPT-J); else
+ *                  KVQ_ERR_UNSUPPORTED.
+ *   positions      int64 [num_tokens], 8-byte aligned, each < max_pos.
+ *
+ * Per head row x (fp32 arithmetic, one bf16 round-to-nearest-even at the end):
+ *   r = 1 / sqrt(sum(x^2) / head_dim + eps);  n_i = x_i * r * w_i
+ *   for each rotated pair (a, b) with frequency index i:
+ *     out_a = n_a * cos_i - n_b * sin_i,   out_b = n_b * cos_i + n_a * sin_i
+ * so the partner enters with its own dimension's weight.  head_dim 128 with
+ * full NeoX rotation runs a tuned kernel; the other layouts a general one.
+ * Source: InfiniOps PR #1019, "Summary" (the API carries is_neox, following
+ * vLLM's fused_qk_norm_rope) and "Notes for Reviewers" (the fast path the
+ * page guards to: bf16, head_dim 128, full-dimension NeoX).
+ */
+kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
+                                 int num_heads_k, int num_heads_v, int head_dim,
+                                 float eps, const void* q_weight,
+                                 const void* k_weight, const float* cos_sin_cache,
+                                 int rotary_dim, int is_neox,
+                                 const int64_t* positions, kvq_stream_t stream);
 
 /*
  * dsv4_qnorm_rope_kv_rope_quant_insert -- q in place, cache entries written.

@@ -46,6 +46,9 @@ _F = ctypes.c_float
 def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fused_qk_norm_rope.restype = _I
     L.fused_qk_norm_rope.argtypes = [_P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P]
+    L.fused_qk_norm_rope_ex.restype = _I
+    L.fused_qk_norm_rope_ex.argtypes = [_P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _I, _I, _P,
+                                        _P]
     L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = _I
     L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [_P, _P, _I64, _I, _F, _P, _P, _P, _P,
                                                        _P, _P, _I, _P]
@@ -120,22 +123,30 @@ def _stream(stream, device) -> int:
 
 def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
                        q_weight, k_weight, cos_sin_cache, is_neox, positions,
-                       stream=None) -> None:
-    """In-place per-head RMSNorm + NeoX RoPE of the Q and K heads of ``qkv``.
+                       stream=None, rotary_dim=None) -> None:
+    """In-place per-head RMSNorm + RoPE of the Q and K heads of ``qkv``.
 
     qkv: bf16 [T, (Hq+Hk+Hv)*head_dim]; weights bf16 [head_dim]; cos_sin_cache
-    fp32 [max_pos, head_dim]; positions int64 [T].  Same parameter order as
+    fp32 [max_pos, rotary_dim]; positions int64 [T].  Same parameter order as
     the C entry point (stream last, default: torch's current stream).
+    ``rotary_dim`` (default: the cos/sin table's width) selects partial
+    rotation through ``fused_qk_norm_rope_ex``; ``is_neox`` picks NeoX (True)
+    or GPT-J (False) pairs.
     """
     if qkv.dim() != 2 or qkv.shape[1] != (num_heads_q + num_heads_k + num_heads_v) * head_dim:
         raise ValueError("qkv must be [T, (Hq+Hk+Hv)*head_dim]")
+    if rotary_dim is None:
+        rotary_dim = cos_sin_cache.shape[1]
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rotary_dim:
+        raise ValueError("cos_sin_cache must be [max_pos, rotary_dim]")
     T = qkv.shape[0]
-    st = lib().fused_qk_norm_rope(
+    st = lib().fused_qk_norm_rope_ex(
         _cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
         head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
         _cuda(k_weight, torch.bfloat16, "k_weight"),
-        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"), int(bool(is_neox)),
-        _cuda(positions, torch.int64, "positions"), _stream(stream, qkv.device))
+        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"), int(rotary_dim),
+        int(bool(is_neox)), _cuda(positions, torch.int64, "positions"),
+        _stream(stream, qkv.device))
     _check(st, "fused_qk_norm_rope")
 
 

@@ -101,15 +101,18 @@ int device_sm_count() {
 
 extern "C" {
 
-kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
-                              int num_heads_k, int num_heads_v, int head_dim,
-                              float eps, const void* q_weight,
-                              const void* k_weight, const float* cos_sin_cache,
-                              int is_neox, const int64_t* positions,
-                              kvq_stream_t stream) {
+kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
+                                 int num_heads_k, int num_heads_v, int head_dim,
+                                 float eps, const void* q_weight,
+                                 const void* k_weight, const float* cos_sin_cache,
+                                 int rotary_dim, int is_neox,
+                                 const int64_t* positions, kvq_stream_t stream) {
   if (num_tokens < 0 || num_heads_q < 0 || num_heads_k < 0 || num_heads_v < 0)
     return KVQ_ERR_SHAPE;
-  if (head_dim != 128 || is_neox != 1) return KVQ_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (is_neox != 0 && is_neox != 1) return KVQ_ERR_UNSUPPORTED;
+  if (rotary_dim < 16 || rotary_dim > head_dim || rotary_dim % 16 != 0)
+    return KVQ_ERR_UNSUPPORTED;
   if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
   const int rows = num_heads_q + num_heads_k;
   if ((int64_t)rows + num_heads_v > (1 << 20) || num_tokens * (int64_t)(rows + 1) >= kIndexLimit)
@@ -129,9 +132,26 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
   a.num_heads_q = num_heads_q;
   a.num_heads_k = num_heads_k;
   a.num_heads_v = num_heads_v;
+  a.head_dim = head_dim;
+  a.rotary_dim = rotary_dim;
+  a.is_neox = is_neox;
   a.eps = eps;
-  return finish_launch(kvq::launch_qk_norm_rope(a, qk_config_for(num_tokens, rows),
-                                                 reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (head_dim == 128 && is_neox == 1 && rotary_dim == 128)
+    return finish_launch(kvq::launch_qk_norm_rope(a, qk_config_for(num_tokens, rows), st));
+  return finish_launch(
+      kvq::launch_qk_general(a, num_tokens * (int64_t)rows < kQkSmallRows, st));
+}
+
+kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
+                              int num_heads_k, int num_heads_v, int head_dim,
+                              float eps, const void* q_weight,
+                              const void* k_weight, const float* cos_sin_cache,
+                              int is_neox, const int64_t* positions,
+                              kvq_stream_t stream) {
+  return fused_qk_norm_rope_ex(qkv, num_tokens, num_heads_q, num_heads_k, num_heads_v,
+                               head_dim, eps, q_weight, k_weight, cos_sin_cache, head_dim,
+                               is_neox, positions, stream);
 }
 
 kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
@@ -171,7 +191,7 @@ const char* kvq_status_string(kvq_status status) {
     case KVQ_OK: return "ok";
     case KVQ_ERR_NULL: return "a required pointer is NULL";
     case KVQ_ERR_SHAPE: return "invalid count or size";
-    case KVQ_ERR_UNSUPPORTED: return "unsupported head_dim / rotary layout";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported head_dim / rotary_dim / is_neox";
     case KVQ_ERR_ALIGN: return "pointer not aligned as required";
     case KVQ_ERR_CUDA: return "CUDA launch failed (see kvq_last_cuda_error)";
     case KVQ_ERR_VALUE: return "eps must be finite and non-negative";

@@ -17,6 +17,7 @@ struct QkArgs {
   const int64_t* positions;
   int num_tokens;
   int num_heads_q, num_heads_k, num_heads_v;
+  int head_dim, rotary_dim, is_neox;
   float eps;
 };
 
@@ -44,7 +45,10 @@ extern const int kQkNumConfigs;
 extern const LaunchConfig kDsv4Configs[];
 extern const int kDsv4NumConfigs;
 
+// Tuned kernel: head_dim 128, full-dimension NeoX rotation.
 cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream);
+// Every other supported layout (head_dim 64/128/256, NeoX or GPT-J, partial).
+cudaError_t launch_qk_general(const QkArgs& a, bool small, cudaStream_t stream);
 cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream);
 
 // Streaming multiprocessors of the current device (cached per device).

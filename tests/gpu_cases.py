@@ -28,9 +28,13 @@ def qk_parity(d, slice_tokens=4096, call=None) -> Bf16Report:
     """d: inputs on the GPU (make_qk ... device=cuda).  Runs the op in place,
     then compares every token with the oracle.  V must be bit-identical."""
     Hq, Hk, Hv, D = d["Hq"], d["Hk"], d["Hv"], d["D"]
+    rot, neox = d.get("rot", D), d.get("is_neox", True)
     qkv_in = d["qkv"].clone()
-    (call or kvq.fused_qk_norm_rope)(d["qkv"], Hq, Hk, Hv, D, d["eps"], d["q_weight"],
-                                     d["k_weight"], d["cos_sin"], True, d["positions"])
+    if call is None:
+        kvq.fused_qk_norm_rope(d["qkv"], Hq, Hk, Hv, D, d["eps"], d["q_weight"], d["k_weight"],
+                               d["cos_sin"], neox, d["positions"], rotary_dim=rot)
+    else:
+        call(d)
     torch.cuda.synchronize()
     qw, kw = wl.bf16_bits(d["q_weight"]), wl.bf16_bits(d["k_weight"])
     cs, pos = wl.host(d["cos_sin"]), wl.host(d["positions"])
@@ -42,7 +46,8 @@ def qk_parity(d, slice_tokens=4096, call=None) -> Bf16Report:
         inp = wl.bf16_bits(qkv_in[a:b])
         gpu = wl.bf16_bits(d["qkv"][a:b]).reshape(b - a, NR + Hv, D)
         out, ref, mag = oracle.qk_norm_rope(inp, Hq, Hk, Hv, D, d["eps"], qw, kw, cs,
-                                            np.ascontiguousarray(pos[a:b]), want_ref=True)
+                                            np.ascontiguousarray(pos[a:b]), is_neox=neox,
+                                            rot_dim=rot, want_ref=True)
         assert np.array_equal(gpu[:, NR:], inp.reshape(b - a, NR + Hv, D)[:, NR:]), "V changed"
         rep.add(gpu[:, :NR], out.reshape(b - a, NR + Hv, D)[:, :NR], ref, mag)
     rep.check("fused_qk_norm_rope")

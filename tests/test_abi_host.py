@@ -51,12 +51,34 @@ A16 = 0x10000
 MIS = 0x10008  # 8-byte but not 16-byte aligned
 
 
-def qk(L, qkv=A16, T=4, hq=2, hk=1, hv=1, d=128, eps=1e-6, qw=A16, kw=A16, cs=A16, neox=1, pos=A16):
-    return L.fused_qk_norm_rope(qkv, T, hq, hk, hv, d, eps, qw, kw, cs, neox, pos, None)
+def _qk_invalid(qkv, T, hq, hk, hv, d, eps, qw, kw, cs, neox, pos, rot):
+    """True when the documented validation rejects these arguments (or there
+    is nothing to do), i.e. when the call cannot reach a kernel launch."""
+    import math
+    ptrs = (qkv, qw, kw, cs, pos)
+    return (T <= 0 or min(hq, hk, hv) < 0 or hq + hk == 0 or d not in (64, 128, 256)
+            or neox not in (0, 1) or rot < 16 or rot > d or rot % 16
+            or not math.isfinite(eps) or eps < 0 or T * (hq + hk + 1) >= 2**31
+            or any(p is None for p in ptrs)
+            or any(p % a for p, a in zip(ptrs, (16, 16, 16, 16, 8))))
+
+
+def qk(L, qkv=A16, T=4, hq=2, hk=1, hv=1, d=128, eps=1e-6, qw=A16, kw=A16, cs=A16, neox=1,
+       pos=A16, rot=None):
+    rot = d if rot is None else rot
+    # fake addresses must never reach a launch
+    assert _qk_invalid(qkv, T, hq, hk, hv, d, eps, qw, kw, cs, neox, pos, rot)
+    return L.fused_qk_norm_rope_ex(qkv, T, hq, hk, hv, d, eps, qw, kw, cs, rot, neox, pos, None)
 
 
 def dsv4(L, q=A16, kv=A16, T=4, H=2, eps=1e-6, qw=A16, kvw=A16, cs=A16, pos=A16, slot=A16,
          cache=A16, bs=64):
+    import math
+    ptrs = (q, kv, qw, kvw, cs, pos, slot, cache)
+    invalid = (T <= 0 or H < 1 or bs < 1 or T * (H + 1) >= 2**31 or not math.isfinite(eps)
+               or eps < 0 or any(p is None for p in ptrs)
+               or any(p % a for p, a in zip(ptrs, (16, 16, 16, 16, 16, 8, 8, 8))))
+    assert invalid  # fake addresses must never reach a launch
     return L.dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, T, H, eps, qw, kvw, cs, pos, slot, cache,
                                                   bs, None)
 
@@ -66,8 +88,18 @@ def test_qk_validation(L):
     assert qk(L, pos=None) == kvq.KVQ_ERR_NULL
     assert qk(L, T=-1) == kvq.KVQ_ERR_SHAPE
     assert qk(L, hq=-1) == kvq.KVQ_ERR_SHAPE
-    assert qk(L, d=64) == kvq.KVQ_ERR_UNSUPPORTED
-    assert qk(L, neox=0) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, d=96) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, d=512) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, neox=2) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, rot=8) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, rot=24) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, d=64, rot=128) == kvq.KVQ_ERR_UNSUPPORTED
+    assert qk(L, rot=0) == kvq.KVQ_ERR_UNSUPPORTED
+    # the plain entry point validates the same way (rotary_dim = head_dim)
+    assert L.fused_qk_norm_rope(A16, 4, 2, 1, 1, 96, 1e-6, A16, A16, A16, 1, A16,
+                                None) == kvq.KVQ_ERR_UNSUPPORTED
+    assert L.fused_qk_norm_rope(A16, 4, 2, 1, 1, 128, 1e-6, A16, A16, A16, 3, A16,
+                                None) == kvq.KVQ_ERR_UNSUPPORTED
     assert qk(L, eps=-1.0) == kvq.KVQ_ERR_VALUE
     assert qk(L, eps=float("nan")) == kvq.KVQ_ERR_VALUE
     assert qk(L, eps=float("inf")) == kvq.KVQ_ERR_VALUE
@@ -78,6 +110,10 @@ def test_qk_validation(L):
     # nothing to do: OK without a launch, even with NULL pointers
     assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, T=0) == kvq.KVQ_OK
     assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, hq=0, hk=0) == kvq.KVQ_OK
+    # valid layouts still reach the pointer checks (and stop there)
+    for d, rot, neox in ((64, 64, 0), (256, 128, 1), (128, 32, 0), (64, 16, 1)):
+        assert qk(L, d=d, rot=rot, neox=neox, qkv=None) == kvq.KVQ_ERR_NULL
+        assert qk(L, d=d, rot=rot, neox=neox, qkv=MIS) == kvq.KVQ_ERR_ALIGN
 
 
 def test_dsv4_validation(L):

@@ -97,3 +97,27 @@ def test_every_launch_config(cuda_device, config, shape):
     d = wl.make_qk(T, Hq, Hk, Hv, theta=1e6, max_pos=131072, seed=31 + config, device=cuda_device)
     with with_config("qk", config):
         qk_parity(d)
+
+
+LAYOUTS = [(D, rot, neox) for D in (64, 128, 256) for neox in (True, False)
+           for rot in sorted({16, D // 2, D}) if rot % 16 == 0 and not (D == 128 and rot == 128 and neox)]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: f"D{l[0]}_rot{l[1]}_{'neox' if l[2] else 'gptj'}")
+@pytest.mark.parametrize("shape", [(1, 4, 2, 1), (17, 3, 1, 2), (777, 8, 2, 2), (300, 0, 5, 0)])
+def test_general_layouts(cuda_device, layout, shape):
+    """head_dim 64/128/256, NeoX or GPT-J pairs, full or partial rotation,
+    through the general kernel, against the oracle."""
+    D, rot, neox = layout
+    T, Hq, Hk, Hv = shape
+    d = wl.make_qk(T, Hq, Hk, Hv, D=D, theta=1e4, max_pos=8192, seed=D + rot + T,
+                   device=cuda_device, rotary_dim=rot, is_neox=neox)
+    qk_parity(d)
+
+
+def test_general_layout_at_scale(cuda_device):
+    """A 32768-token partial-rotation GPT-J case (the general kernel's large
+    launch), every token against the oracle."""
+    d = wl.make_qk(32768, 16, 4, 4, D=256, theta=1e6, max_pos=131072, seed=77,
+                   device=cuda_device, rotary_dim=64, is_neox=False)
+    qk_parity(d, slice_tokens=8192)

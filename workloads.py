@@ -124,8 +124,10 @@ def _normal_bf16(shape, g, device, mean=0.0, std=1.0) -> torch.Tensor:
 
 
 def make_qk(T, Hq, Hk, Hv, D=128, theta=1e4, max_pos=4096, positions="uniform",
-            seed=0, device="cpu", eps=EPS):
-    """Inputs of the packed-QKV operator as a dict of tensors on ``device``."""
+            seed=0, device="cpu", eps=EPS, rotary_dim=None, is_neox=True):
+    """Inputs of the packed-QKV operator as a dict of tensors on ``device``.
+    The cos/sin table has ``rotary_dim`` columns (default: the head dim)."""
+    rot = D if rotary_dim is None else rotary_dim
     g = _gen(seed, device)
     qkv = _normal_bf16((T, (Hq + Hk + Hv) * D), g, device)
     q_weight = _normal_bf16((D,), g, device, 1.0, 0.1)
@@ -135,8 +137,8 @@ def make_qk(T, Hq, Hk, Hv, D=128, theta=1e4, max_pos=4096, positions="uniform",
     else:
         pos = torch.randint(0, max_pos, (T,), generator=g, device=device, dtype=torch.int64)
     return dict(qkv=qkv, q_weight=q_weight, k_weight=k_weight,
-                cos_sin=cos_sin_table(max_pos, D, theta, device), positions=pos,
-                Hq=Hq, Hk=Hk, Hv=Hv, D=D, eps=eps)
+                cos_sin=cos_sin_table(max_pos, rot, theta, device), positions=pos,
+                Hq=Hq, Hk=Hk, Hv=Hv, D=D, eps=eps, rot=rot, is_neox=is_neox)
 
 
 def make_qk_workload(w: QKWorkload, device="cpu"):
