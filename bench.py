@@ -581,6 +581,20 @@ def sweep(kvq, device):
         nb = dsv4_bytes(w.T, w.H, int((d["slot_mapping"] >= 0).sum()))
         run_configs("dsv4", w.name, nb, lambda: launch_dsv4(kvq, d, stream), 30 if nb < 2**32 else 8)
         del d
+    # reading entries back: random slots of a full 65536-slot cache
+    for n in (16, 32768, 131072):
+        d = wl.make_dsv4_workload(wl.DSV4_LARGE, device=device)
+        launch_dsv4(kvq, d, stream)
+        slots = torch.randint(0, 65536, (n,), device=device, dtype=torch.int64)
+        rows = torch.empty((n, 512), dtype=torch.bfloat16, device=device)
+        nb = n * (584 + 8 + 1024)
+        small = nb < 256 * 2**20
+        med, _ = _time_launch(lambda: kvq.dsv4_kv_cache_gather(d["kv_cache"], slots, rows, stream),
+                              30, stream, flush if small else None)
+        emit({"sweep": f"gather_n{n}", "config": "gather", "bytes": nb,
+              "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
+              "pct_peak": round(100 * nb / med / 1e6 / peak, 1), "l2_flush": small})
+        del d
     # dispatch crossover between the small- and large-batch shapes
     for H in (64, 128):
         for T in (1, 4, 16, 64, 128, 256, 512, 1024, 4096):

@@ -171,6 +171,27 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
     const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
     int block_size, kvq_stream_t stream);
 
+/*
+ * dsv4_kv_cache_gather -- read cache entries back as bf16 rows (the consumer
+ * side of dsv4_qnorm_rope_kv_rope_quant_insert, e.g. for attention).
+ *
+ *   kv_cache   uint8 [num_blocks, block_size, 584], 8-byte aligned (layout as
+ *              written by the insert above); read only.
+ *   block_size >= 1.
+ *   slots      int64 [num_rows], 8-byte aligned; each -1 or a slot inside
+ *              the cache (not checked).
+ *   num_rows   >= 0 and below 2^31.
+ *   out        bf16 [num_rows, 512], 16-byte aligned, written:
+ *                dims 64b + k (b < 7): e4m3(code) * 2^(byte_b - 127), rounded
+ *                once to bf16 (exact unless below bf16's range);
+ *                dims 448..511: the stored bf16 rotary values;
+ *                slots[i] == -1: a row of +0.
+ * Source: FlagGems PR #5449, "Performance" (the blockwise UE8M0 layout with
+ * seven per-block exponents per token is the cache format to be read back).
+ */
+kvq_status dsv4_kv_cache_gather(const uint8_t* kv_cache, int block_size, const int64_t* slots,
+                                int64_t num_rows, void* out, kvq_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char* kvq_status_string(kvq_status status);
 

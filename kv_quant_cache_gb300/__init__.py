@@ -52,6 +52,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = _I
     L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [_P, _P, _I64, _I, _F, _P, _P, _P, _P,
                                                        _P, _P, _I, _P]
+    L.dsv4_kv_cache_gather.restype = _I
+    L.dsv4_kv_cache_gather.argtypes = [_P, _I, _P, _I64, _P, _P]
     L.kvq_status_string.restype = ctypes.c_char_p
     L.kvq_status_string.argtypes = [_I]
     L.kvq_last_cuda_error.restype = _I
@@ -170,6 +172,24 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
         _cuda(positions, torch.int64, "positions"), _cuda(slot_mapping, torch.int64, "slot_mapping"),
         _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1], _stream(stream, q.device))
     _check(st, "dsv4_qnorm_rope_kv_rope_quant_insert")
+
+
+def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None):
+    """bf16 [n, 512] rows read back from the cache entries at ``slots``
+    (int64 [n], -1 = a zero row); ``out`` is allocated if not given."""
+    if kv_cache.dim() != 3 or kv_cache.shape[2] != ENTRY_BYTES:
+        raise ValueError("kv_cache must be [num_blocks, block_size, 584]")
+    n = slots.shape[0]
+    if out is None:
+        out = torch.empty((n, DSV4_DIM), dtype=torch.bfloat16, device=kv_cache.device)
+    if out.shape != (n, DSV4_DIM):
+        raise ValueError("out must be [len(slots), 512]")
+    st = lib().dsv4_kv_cache_gather(
+        _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1],
+        _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
+        _stream(stream, kv_cache.device))
+    _check(st, "dsv4_kv_cache_gather")
+    return out
 
 
 def dsv4_dispatch_threshold() -> int:

@@ -186,6 +186,20 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status dsv4_kv_cache_gather(const uint8_t* kv_cache, int block_size, const int64_t* slots,
+                                int64_t num_rows, void* out, kvq_stream_t stream) {
+  if (num_rows < 0 || num_rows >= kIndexLimit || block_size < 1) return KVQ_ERR_SHAPE;
+  if (num_rows == 0) return KVQ_OK;
+  if (!kv_cache || !slots || !out) return KVQ_ERR_NULL;
+  if (!aligned(kv_cache, 8) || !aligned(slots, 8) || !aligned(out, 16)) return KVQ_ERR_ALIGN;
+  kvq::GatherArgs a;
+  a.kv_cache = kv_cache;
+  a.slots = slots;
+  a.out = out;
+  a.num_rows = (int)num_rows;
+  return finish_launch(kvq::launch_dsv4_gather(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* kvq_status_string(kvq_status status) {
   switch (status) {
     case KVQ_OK: return "ok";

@@ -35,6 +35,13 @@ struct Dsv4Args {
   float eps;
 };
 
+struct GatherArgs {
+  const uint8_t* kv_cache;
+  const int64_t* slots;
+  void* out;
+  int num_rows;
+};
+
 // A launch shape of one operator (an instantiation of one of its kernels).
 struct LaunchConfig {
   const char* name;
@@ -50,6 +57,7 @@ cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream
 // Every other supported layout (head_dim 64/128/256, NeoX or GPT-J, partial).
 cudaError_t launch_qk_general(const QkArgs& a, bool small, cudaStream_t stream);
 cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream);
+cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream);
 
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();

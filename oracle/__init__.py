@@ -77,6 +77,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_qk_norm_rope.restype = _I
     lib.orc_qk_norm_rope.argtypes = [_P, _P, _I64, _I, _I, _I, _I, ctypes.c_float,
                                      _P, _P, _P, _I64, _I, _I, _P, _P, _P, _I]
+    lib.orc_dsv4_gather.restype = _I
+    lib.orc_dsv4_gather.argtypes = [_P, _I64, _I, _P, _I64, _P]
     lib.orc_dsv4.restype = _I
     lib.orc_dsv4.argtypes = [_P, _P, _P, _I64, _I, ctypes.c_float, _P, _P, _P, _I64,
                              _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _I]
@@ -209,3 +211,16 @@ def dsv4(q, kv, eps, q_weight, kv_weight, cos_sin, positions, slot_mapping, kv_c
     if rc != 0:
         raise OracleError(f"orc_dsv4 returned {rc}")
     return res
+
+
+def dsv4_gather(kv_cache, slots, _lib=None):
+    """bf16 bits [n, 512] read back from the entries at ``slots`` (see oracle.h)."""
+    L = _lib or lib()
+    _need(kv_cache, np.uint8, "kv_cache")
+    _need(slots, np.int64, "slots")
+    out = np.empty((slots.size, DSV4_DIM), np.uint16)
+    rc = L.orc_dsv4_gather(_ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(slots),
+                           slots.size, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"orc_dsv4_gather returned {rc}")
+    return out

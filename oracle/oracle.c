@@ -410,3 +410,35 @@ int orc_dsv4(const uint16_t* q_in, uint16_t* q_out, const uint16_t* kv,
                  q_ref, q_mag, kv_ref, kv_mag, exp_margin};
   return run_tokens(dsv4_token, &A, T, nthreads);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Reading entries back                                                      */
+/* ------------------------------------------------------------------------ */
+
+int orc_dsv4_gather(const uint8_t* kv_cache, int64_t num_blocks, int block_size,
+                    const int64_t* slots, int64_t n, uint16_t* out) {
+  if (n < 0 || block_size <= 0 || num_blocks < 0) return -2;
+  if (n == 0) return 0;
+  if (!kv_cache || !slots || !out) return -1;
+  const int64_t num_slots = num_blocks * (int64_t)block_size;
+  for (int64_t i = 0; i < n; ++i) {
+    uint16_t* row = out + i * DSV4_DIM;
+    const int64_t s = slots[i];
+    if (s < 0) {
+      memset(row, 0, DSV4_DIM * sizeof(uint16_t));
+      continue;
+    }
+    if (s >= num_slots) return -4;
+    const int64_t blk = s / block_size, off = s % block_size;
+    const uint8_t* e = kv_cache + (blk * block_size + off) * (int64_t)DSV4_ENTRY;
+    for (int b = 0; b < DSV4_NBLOCK; ++b) {
+      const int ex = (int)e[DSV4_SCALE_AT + b] - 127;
+      for (int j = 0; j < DSV4_BLOCK; ++j)
+        row[b * DSV4_BLOCK + j] = orc_bf16_round(ldexp(orc_e4m3_value(e[b * DSV4_BLOCK + j]), ex));
+    }
+    for (int i2 = 0; i2 < DSV4_ROPE; ++i2)
+      row[DSV4_ROPE_OFF + i2] =
+          (uint16_t)(e[DSV4_ROPE_AT + 2 * i2] | ((uint16_t)e[DSV4_ROPE_AT + 2 * i2 + 1] << 8));
+  }
+  return 0;
+}

@@ -130,6 +130,16 @@ int orc_dsv4(const uint16_t* q_in, uint16_t* q_out, const uint16_t* kv,
              double* q_ref, double* q_mag, double* kv_ref, double* kv_mag,
              double* exp_margin, int nthreads);
 
+/*
+ * Read cache entries back (the consumer side of the DSV4 insert): row i of
+ * `out` (bf16 bits [n, 512]) is the entry at slot slots[i]: dims 64b+k
+ * (b < 7) = bf16(e4m3_value(code) * 2^(byte_b - 127)), one rounding; dims
+ * 448..511 = the stored bf16 values; slots[i] < 0 gives a row of +0.
+ * Returns 0, -1 null, -2 shape, -4 slot out of range.
+ */
+int orc_dsv4_gather(const uint8_t* kv_cache, int64_t num_blocks, int block_size,
+                    const int64_t* slots, int64_t n, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

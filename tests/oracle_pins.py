@@ -456,6 +456,37 @@ def pin_slicing_and_threads(L):
     assert np.array_equal(np.concatenate(qs), full["q"]) and np.array_equal(cache, full["cache"])
 
 
+def pin_gather_hand_entry(L):
+    """The hand-derived entry reads back as the block weights exactly:
+    0x78 = 256, 0x7c = 384, 0x7a = 320 times 2^(byte - 127)."""
+    cache = np.full((3, 4, 584), wl.SENTINEL, np.uint8)
+    cache.reshape(-1)[5 * 584:6 * 584] = _hand_entry()
+    out = oracle.dsv4_gather(cache, np.array([5, -1], np.int64), _lib=L)
+    want = np.repeat([1.0, 2.0, 4.0, 8.0, 0.5, 3.0, 5.0, 1.0], 64)
+    assert np.array_equal(_bf16_value(out[0]), want)
+    assert np.all(out[1] == 0)
+
+
+def pin_gather_round_trip(L):
+    """Insert then read back: each dequantised value is within half an e4m3
+    step of the fp32 value the codes were taken from (2^-4 relative for
+    normal codes, 2^(e-10) absolute below), and the rotary dims come back as
+    the nearest bf16 of the exact values."""
+    T = 16
+    inp = _dsv4_inputs(T, 1, num_blocks=8, block_size=4)
+    r = _run_dsv4(L, inp)
+    out = oracle.dsv4_gather(r["cache"], inp["slot_mapping"], _lib=L)
+    got = _bf16_value(out)
+    ent = r["cache"].reshape(-1, 584)[inp["slot_mapping"]]
+    e = ent[:, 576:583].astype(np.int64) - 127
+    f32 = r["kv_ref"][:, :448].astype(np.float32).astype(np.float64).reshape(T, 7, 64)
+    scale = np.ldexp(1.0, e)[:, :, None]
+    err = np.abs(got[:, :448].reshape(T, 7, 64) - f32)
+    bound = np.maximum(np.abs(f32) * 2.0 ** -4, scale * 2.0 ** -10)
+    assert np.all(err <= bound * (1 + 1e-12))
+    assert _is_nearest_bf16(out[:, 448:], r["kv_ref"][:, 448:]).all()
+
+
 ALL_PINS = [
     pin_bf16_value_and_roundtrip, pin_bf16_vs_torch, pin_bf16_single_rounding,
     pin_e4m3_decode_vs_torch, pin_e4m3_roundtrip, pin_e4m3_vs_torch,
@@ -463,5 +494,5 @@ ALL_PINS = [
     pin_qk_textbook_rmsnorm, pin_qk_all_equal_row, pin_qk_rope_complex,
     pin_qk_partner_weight, pin_qk_pairing_index, pin_qk_v_untouched,
     pin_dsv4_hand_entry, pin_dsv4_skip_and_addressing, pin_dsv4_q_textbook,
-    pin_dsv4_kv_decisions, pin_slicing_and_threads,
+    pin_dsv4_kv_decisions, pin_slicing_and_threads, pin_gather_hand_entry, pin_gather_round_trip,
 ]

@@ -197,3 +197,19 @@ def test_launch_config_table(L):
         kvq.set_config("dsv4", -1)
     assert kvq.dsv4_config_for(1, 1) in range(len(kvq.configs("dsv4")))
     assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))
+
+
+def test_gather_validation(L):
+    def g(cache=A16, bs=64, slots=A16, n=4, out=A16):
+        ptrs = (cache, slots, out)
+        assert (n <= 0 or bs < 1 or any(p is None for p in ptrs)
+                or any(p % a for p, a in zip(ptrs, (8, 8, 16))))  # never a launch
+        return L.dsv4_kv_cache_gather(cache, bs, slots, n, out, None)
+    assert g(cache=None) == kvq.KVQ_ERR_NULL
+    assert g(out=None) == kvq.KVQ_ERR_NULL
+    assert g(n=-1) == kvq.KVQ_ERR_SHAPE
+    assert g(bs=0) == kvq.KVQ_ERR_SHAPE
+    assert g(cache=A16 + 4) == kvq.KVQ_ERR_ALIGN
+    assert g(out=A16 + 8) == kvq.KVQ_ERR_ALIGN
+    assert g(slots=A16 + 4) == kvq.KVQ_ERR_ALIGN
+    assert g(cache=None, slots=None, out=None, n=0) == kvq.KVQ_OK

@@ -152,3 +152,62 @@ def test_every_launch_config(cuda_device, config, shape):
                      slots="distinct_skip2", seed=300 + config, device=cuda_device)
     with with_config("dsv4", config):
         dsv4_parity(d)
+
+
+# ---- reading entries back (dsv4_kv_cache_gather) ---------------------------
+
+def _gather_vs_oracle(cache_dev, slots):
+    import oracle
+    out = kvq.dsv4_kv_cache_gather(cache_dev, slots)
+    torch.cuda.synchronize()
+    want = oracle.dsv4_gather(wl.host(cache_dev), wl.host(slots))
+    got = wl.bf16_bits(out)
+    assert np.array_equal(got, want), f"{int((got != want).sum())} values differ"
+    return got
+
+
+@pytest.mark.parametrize("T,H", [(16, 64), (777, 3), (8192, 8)])
+def test_gather_after_insert(cuda_device, T, H):
+    """Insert on the GPU, read the entries back on the GPU: bit-exact against
+    the oracle's reading of the same cache bytes, and within half an e4m3 step
+    of the oracle's exact normalised values."""
+    import oracle
+    d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 64), block_size=64,
+                     slots="distinct_skip2", seed=500 + T, device=cuda_device)
+    q_in, cache_in = wl.bf16_bits(d["q"]), wl.host(d["kv_cache"]).copy()
+    run_dsv4(d)
+    slots = d["slot_mapping"]
+    got = _gather_vs_oracle(d["kv_cache"], slots)
+    res = oracle.dsv4(q_in, wl.bf16_bits(d["kv"]), d["eps"], wl.bf16_bits(d["q_weight"]),
+                      wl.bf16_bits(d["kv_weight"]), wl.host(d["cos_sin"]), wl.host(d["positions"]),
+                      wl.host(slots), cache_in, want_ref=True)
+    m = wl.host(slots) >= 0
+    vals = (got[m].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    n32 = res["kv_ref"][m].astype(np.float32).astype(np.float64)
+    ent = wl.host(d["kv_cache"]).reshape(-1, 584)[wl.host(slots)[m]]
+    scale = np.ldexp(1.0, ent[:, 576:583].astype(np.int64) - 127)
+    err = np.abs(vals[:, :448] - n32[:, :448]).reshape(-1, 7, 64)
+    bound = np.maximum(np.abs(n32[:, :448]).reshape(-1, 7, 64) * 2.0 ** -4,
+                       scale[:, :, None] * 2.0 ** -10)
+    assert np.all(err <= bound * (1 + 2.0 ** -10) + 1e-30)
+    assert np.all(got[~m] == 0)
+
+
+def test_gather_repeated_and_edge_slots(cuda_device):
+    d = wl.make_dsv4(64, 2, max_pos=4096, num_blocks=2, block_size=64, seed=9, device=cuda_device)
+    run_dsv4(d)
+    slots = torch.tensor([0, 127, -1, 5, 5, 127, -1], dtype=torch.int64, device=cuda_device)
+    _gather_vs_oracle(d["kv_cache"], slots)
+
+
+def test_gather_hand_entry(cuda_device):
+    """The hand-derived entry reads back as the block weights."""
+    block_w = [1.0, 2.0, 4.0, 8.0, 0.5, 3.0, 5.0]
+    codes = [0x78] * (5 * 64) + [0x7C] * 64 + [0x7A] * 64
+    entry = np.array(codes + [0x80, 0x3F] * 64 + [119, 120, 121, 122, 118, 120, 121, 0], np.uint8)
+    cache = np.full((1, 4, 584), 0xA5, np.uint8)
+    cache.reshape(-1)[2 * 584:3 * 584] = entry
+    out = kvq.dsv4_kv_cache_gather(torch.from_numpy(cache).to(cuda_device),
+                                   torch.tensor([2], dtype=torch.int64, device=cuda_device))
+    assert torch.equal(out[0].float().cpu(),
+                       torch.tensor(np.repeat(block_w + [1.0], 64), dtype=torch.float32))

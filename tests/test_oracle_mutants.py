@@ -48,6 +48,10 @@ MUTANTS = {
     # (kept inside the cache: a mutant must not write out of bounds)
     "slot_hardcoded_block": ("(blk * A->block_size + off)", "((blk * 64 + off) % A->num_slots)"),
     "skip_ignored": ("const int64_t s = A->slot[t];", "const int64_t s = A->slot[t] < 0 ? 0 : A->slot[t];"),
+    "gather_scale_bias": ("const int ex = (int)e[DSV4_SCALE_AT + b] - 127;",
+                          "const int ex = (int)e[DSV4_SCALE_AT + b] - 126;"),
+    "gather_block_scale": ("const int ex = (int)e[DSV4_SCALE_AT + b] - 127;",
+                           "const int ex = (int)e[DSV4_SCALE_AT] - 127;"),
     "kv_uses_q_weight": ("rms_norm_weight(A->kv + krow, A->kvw,", "rms_norm_weight(A->kv + krow, A->qw,"),
 }
 
