@@ -595,6 +595,33 @@ def sweep(kvq, device):
               "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
               "pct_peak": round(100 * nb / med / 1e6 / peak, 1), "l2_flush": small})
         del d
+    # decode step: 32 layers of (QK 17 tokens + DSV4 16 tokens x 64 heads),
+    # eager launches vs one CUDA graph replay
+    layers = []
+    for i in range(32):
+        qk = wl.make_qk(17, 16, 8, 8, theta=1e4, max_pos=4096, seed=i, device=device)
+        ds = wl.make_dsv4(16, 64, max_pos=65536, num_blocks=64, block_size=64,
+                          slots="distinct_skip2", seed=i, device=device)
+        layers.append((qk, ds))
+
+    def decode_step(st):
+        for qk, ds in layers:
+            launch_qk(kvq, qk, st)
+            launch_dsv4(kvq, ds, st)
+    decode_step(stream)
+    torch.cuda.synchronize()
+    eager_ms, _ = _time_launch(lambda: decode_step(stream), 20, stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode_step(torch.cuda.current_stream(device))
+    graph.replay()
+    torch.cuda.synchronize()
+    graph_ms, _ = _time_launch(graph.replay, 20, stream)
+    emit({"sweep": "decode_32_layers", "eager_us": round(eager_ms * 1e3, 1),
+          "graph_us": round(graph_ms * 1e3, 1),
+          "eager_us_per_launch": round(eager_ms * 1e3 / 64, 2),
+          "graph_us_per_launch": round(graph_ms * 1e3 / 64, 2)})
+    del layers, graph
     # dispatch crossover between the small- and large-batch shapes
     for H in (64, 128):
         for T in (1, 4, 16, 64, 128, 256, 512, 1024, 4096):

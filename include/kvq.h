@@ -40,7 +40,10 @@
  *     no staging copy -- V of the packed QKV tensor never crosses it.  The
  *     library does not check which kind a pointer is.
  *   - All buffers are owned by the caller.  The library allocates no memory,
- *     keeps no per-call state, and never synchronises the stream.
+ *     keeps no per-call state, and never synchronises the stream, so every
+ *     entry point can be recorded into a CUDA graph (stream capture); call
+ *     each operator once on the device before capturing, so that the one
+ *     per-device occupancy query of the large-batch shapes is cached.
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  A KVQ_OK
  *     return means "validated and enqueued"; kernel faults surface on the
  *     stream like any other kernel's.
@@ -74,7 +77,7 @@ typedef enum kvq_status {
   KVQ_ERR_UNSUPPORTED = 3, /* head_dim / rotary_dim / is_neox outside the set above */
   KVQ_ERR_ALIGN = 4,       /* a pointer is not aligned as required below */
   KVQ_ERR_CUDA = 5,        /* the kernel launch itself failed */
-  KVQ_ERR_VALUE = 6        /* eps negative or not finite */
+  KVQ_ERR_VALUE = 6        /* eps negative or not finite; q_out partly overlaps q */
 } kvq_status;
 
 /*
@@ -167,6 +170,19 @@ kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
  */
 kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
     void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int block_size, kvq_stream_t stream);
+
+/*
+ * dsv4_qnorm_rope_kv_rope_quant_insert_out -- the same operator with a
+ * separate q output: q is read only and the normalised, rotated rows go to
+ * q_out (bf16 [num_tokens, num_heads, 512], 16-byte aligned).  q_out == q is
+ * the in-place operator above; a q_out that partly overlaps q is rejected
+ * with KVQ_ERR_VALUE.  Everything else as above.
+ */
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
+    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
     const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
     const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
     int block_size, kvq_stream_t stream);

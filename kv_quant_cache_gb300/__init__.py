@@ -52,6 +52,9 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.dsv4_qnorm_rope_kv_rope_quant_insert.restype = _I
     L.dsv4_qnorm_rope_kv_rope_quant_insert.argtypes = [_P, _P, _I64, _I, _F, _P, _P, _P, _P,
                                                        _P, _P, _I, _P]
+    L.dsv4_qnorm_rope_kv_rope_quant_insert_out.restype = _I
+    L.dsv4_qnorm_rope_kv_rope_quant_insert_out.argtypes = [_P, _P, _P, _I64, _I, _F, _P, _P,
+                                                           _P, _P, _P, _P, _I, _P]
     L.dsv4_kv_cache_gather.restype = _I
     L.dsv4_kv_cache_gather.argtypes = [_P, _I, _P, _I64, _P, _P]
     L.kvq_status_string.restype = ctypes.c_char_p
@@ -154,10 +157,11 @@ def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps
 
 def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_sin_cache,
                                          positions, slot_mapping, kv_cache,
-                                         stream=None) -> None:
-    """DSV4 prologue: q [T,H,512] normalised + rotated in place; the kv
-    vectors [T,512] normalised, rotated, quantised and written to
-    ``kv_cache`` uint8 [num_blocks, block_size, 584] at ``slot_mapping``."""
+                                         stream=None, q_out=None) -> None:
+    """DSV4 prologue: q [T,H,512] normalised + rotated (in place, or into
+    ``q_out`` when given); the kv vectors [T,512] normalised, rotated,
+    quantised and written to ``kv_cache`` uint8 [num_blocks, block_size, 584]
+    at ``slot_mapping``."""
     if q.dim() != 3 or q.shape[2] != DSV4_DIM:
         raise ValueError("q must be [T, H, 512]")
     if kv.dim() != 2 or kv.shape[0] != q.shape[0] or kv.shape[1] != DSV4_DIM:
@@ -165,8 +169,13 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
     if kv_cache.dim() != 3 or kv_cache.shape[2] != ENTRY_BYTES:
         raise ValueError("kv_cache must be [num_blocks, block_size, 584]")
     T, H = q.shape[0], q.shape[1]
-    st = lib().dsv4_qnorm_rope_kv_rope_quant_insert(
-        _cuda(q, torch.bfloat16, "q"), _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
+    if q_out is None:
+        q_out = q
+    if q_out.shape != q.shape:
+        raise ValueError("q_out must have q's shape")
+    st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_out(
+        _cuda(q, torch.bfloat16, "q"), _cuda(q_out, torch.bfloat16, "q_out"),
+        _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
         _cuda(q_weight, torch.bfloat16, "q_weight"), _cuda(kv_weight, torch.bfloat16, "kv_weight"),
         _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"),
         _cuda(positions, torch.int64, "positions"), _cuda(slot_mapping, torch.int64, "slot_mapping"),

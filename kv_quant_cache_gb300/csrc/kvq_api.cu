@@ -154,8 +154,8 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
                                is_neox, positions, stream);
 }
 
-kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
-    void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
+    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
     const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
     const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
     int block_size, kvq_stream_t stream) {
@@ -163,15 +163,21 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
   if (num_tokens * (int64_t)(num_heads + 1) >= kIndexLimit) return KVQ_ERR_SHAPE;
   if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
   if (num_tokens == 0) return KVQ_OK;
-  if (!q || !kv || !q_weight || !kv_weight || !cos_sin_cache || !positions || !slot_mapping ||
-      !kv_cache)
+  if (!q || !q_out || !kv || !q_weight || !kv_weight || !cos_sin_cache || !positions ||
+      !slot_mapping || !kv_cache)
     return KVQ_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(kv_weight, 16) ||
-      !aligned(cos_sin_cache, 16) || !aligned(positions, 8) || !aligned(slot_mapping, 8) ||
-      !aligned(kv_cache, 8))
+  if (!aligned(q, 16) || !aligned(q_out, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) ||
+      !aligned(kv_weight, 16) || !aligned(cos_sin_cache, 16) || !aligned(positions, 8) ||
+      !aligned(slot_mapping, 8) || !aligned(kv_cache, 8))
     return KVQ_ERR_ALIGN;
+  // q_out must be q itself or not overlap it: a partial overlap would let one
+  // warp overwrite rows another warp has not read yet.
+  const uintptr_t qa = reinterpret_cast<uintptr_t>(q), oa = reinterpret_cast<uintptr_t>(q_out);
+  const uintptr_t qbytes = (uintptr_t)num_tokens * (uintptr_t)num_heads * 512u * 2u;
+  if (qa != oa && qa < oa + qbytes && oa < qa + qbytes) return KVQ_ERR_VALUE;
   kvq::Dsv4Args a;
   a.q = q;
+  a.q_out = q_out;
   a.kv = kv;
   a.q_weight = q_weight;
   a.kv_weight = kv_weight;
@@ -184,6 +190,16 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
   a.eps = eps;
   return finish_launch(kvq::launch_dsv4(a, dsv4_config_for(num_tokens, num_heads),
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
+    void* q, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int block_size, kvq_stream_t stream) {
+  return dsv4_qnorm_rope_kv_rope_quant_insert_out(q, q, kv, num_tokens, num_heads, eps,
+                                                  q_weight, kv_weight, cos_sin_cache, positions,
+                                                  slot_mapping, kv_cache, block_size, stream);
 }
 
 kvq_status dsv4_kv_cache_gather(const uint8_t* kv_cache, int block_size, const int64_t* slots,
@@ -208,7 +224,7 @@ const char* kvq_status_string(kvq_status status) {
     case KVQ_ERR_UNSUPPORTED: return "unsupported head_dim / rotary_dim / is_neox";
     case KVQ_ERR_ALIGN: return "pointer not aligned as required";
     case KVQ_ERR_CUDA: return "CUDA launch failed (see kvq_last_cuda_error)";
-    case KVQ_ERR_VALUE: return "eps must be finite and non-negative";
+    case KVQ_ERR_VALUE: return "eps not finite / negative, or q_out partly overlaps q";
   }
   return "unknown kvq_status";
 }

@@ -47,7 +47,8 @@ constexpr int kScaleAt = 576;  // entry offset of the exponent bytes
 constexpr int kRopeLane = 24;  // first lane whose chunk 1 is rotary
 
 struct Dsv4Params {
-  __nv_bfloat16* q;
+  const __nv_bfloat16* q;
+  __nv_bfloat16* q_out;  // equal to q when the operator runs in place
   const __nv_bfloat16* kv;
   const __nv_bfloat16* q_weight;
   const __nv_bfloat16* kv_weight;
@@ -152,7 +153,7 @@ __device__ __forceinline__ void q_row(const Dsv4Params& p, int row, const RowReg
                                       const Weights& w, int lane) {
   float x[16];
   norm_rope(r, w, p.eps, lane, x);
-  __nv_bfloat16* dst = p.q + (size_t)row * kDim;
+  __nv_bfloat16* dst = p.q_out + (size_t)row * kDim;
   store_stream(dst + 8 * lane, pack_bf16x8(x));
   store_stream(dst + 256 + 8 * lane, pack_bf16x8(x + 8));
 }
@@ -281,7 +282,8 @@ dsv4_stream_kernel(const Dsv4Params p) {
 
 Dsv4Params make_params(const Dsv4Args& a) {
   Dsv4Params p;
-  p.q = static_cast<__nv_bfloat16*>(a.q);
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.q_out = static_cast<__nv_bfloat16*>(a.q_out);
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
   p.q_weight = static_cast<const __nv_bfloat16*>(a.q_weight);
   p.kv_weight = static_cast<const __nv_bfloat16*>(a.kv_weight);

@@ -22,7 +22,8 @@ struct QkArgs {
 };
 
 struct Dsv4Args {
-  void* q;
+  const void* q;
+  void* q_out;  // == q for the in-place operator
   const void* kv;
   const void* q_weight;
   const void* kv_weight;

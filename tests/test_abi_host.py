@@ -213,3 +213,18 @@ def test_gather_validation(L):
     assert g(out=A16 + 8) == kvq.KVQ_ERR_ALIGN
     assert g(slots=A16 + 4) == kvq.KVQ_ERR_ALIGN
     assert g(cache=None, slots=None, out=None, n=0) == kvq.KVQ_OK
+
+
+def test_out_of_place_validation(L):
+    def o(q=A16, q_out=A16 + 2**20, kv=A16, T=4, H=2, eps=1e-6):
+        qbytes = T * H * 1024
+        overlap = q is not None and q_out is not None and q != q_out and \
+            q < q_out + qbytes and q_out < q + qbytes
+        assert (q is None or q_out is None or q_out % 16 or overlap or T <= 0)  # no launch
+        return L.dsv4_qnorm_rope_kv_rope_quant_insert_out(q, q_out, kv, T, H, eps, A16, A16, A16,
+                                                          A16, A16, A16, 64, None)
+    assert o(q_out=None) == kvq.KVQ_ERR_NULL
+    assert o(q_out=A16 + 2**20 + 8) == kvq.KVQ_ERR_ALIGN
+    assert o(q_out=A16 + 1024) == kvq.KVQ_ERR_VALUE          # partial overlap
+    assert o(q_out=A16 - 4096) == kvq.KVQ_ERR_VALUE
+    assert o(T=0, q=None, q_out=None) == kvq.KVQ_OK

@@ -211,3 +211,78 @@ def test_gather_hand_entry(cuda_device):
                                    torch.tensor([2], dtype=torch.int64, device=cuda_device))
     assert torch.equal(out[0].float().cpu(),
                        torch.tensor(np.repeat(block_w + [1.0], 64), dtype=torch.float32))
+
+
+# ---- separate q output and CUDA-graph capture -------------------------------
+
+@pytest.mark.parametrize("T,H,threshold", [(16, 64, None), (777, 5, TILED_PATH),
+                                           (777, 5, SMALL_PATH), (4096, 64, None)])
+def test_out_of_place_q(cuda_device, T, H, threshold):
+    """q is read only, q_out receives the rows; against the oracle."""
+    import oracle
+    d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 64), block_size=64,
+                     slots="distinct_skip2", seed=700 + T, device=cuda_device)
+    q_before = d["q"].clone()
+    cache_in = wl.host(d["kv_cache"]).copy()
+    q_out = torch.full_like(d["q"], float("nan"))
+    ctx = with_threshold(threshold) if threshold is not None else with_config("dsv4", -1)
+    with ctx:
+        kvq.dsv4_qnorm_rope_kv_rope_quant_insert(d["q"], d["kv"], d["eps"], d["q_weight"],
+                                                 d["kv_weight"], d["cos_sin"], d["positions"],
+                                                 d["slot_mapping"], d["kv_cache"], q_out=q_out)
+    torch.cuda.synchronize()
+    assert torch.equal(d["q"], q_before)
+    res = oracle.dsv4(wl.bf16_bits(q_before), wl.bf16_bits(d["kv"]), d["eps"],
+                      wl.bf16_bits(d["q_weight"]), wl.bf16_bits(d["kv_weight"]),
+                      wl.host(d["cos_sin"]), wl.host(d["positions"]), wl.host(d["slot_mapping"]),
+                      cache_in, want_ref=True)
+    from parity import Bf16Report, compare_cache
+    rep = Bf16Report()
+    rep.add(wl.bf16_bits(q_out), res["q"], res["q_ref"], res["q_mag"])
+    rep.check("q_out")
+    compare_cache(wl.host(d["kv_cache"]), cache_in, wl.host(d["slot_mapping"]), res["kv_ref"],
+                  res["kv_mag"], res["exp_margin"]).check("cache")
+
+
+def _layer_inputs(dev, i, T_qk=17, T_ds=16):
+    qk = wl.make_qk(T_qk, 16, 8, 8, theta=1e4, max_pos=4096, seed=800 + i, device=dev)
+    ds = wl.make_dsv4(T_ds, 64, max_pos=65536, num_blocks=64, block_size=64,
+                      slots="distinct_skip2", seed=900 + i, device=dev)
+    return qk, ds
+
+
+def _run_layer(qk, ds):
+    kvq.fused_qk_norm_rope(qk["qkv"], 16, 8, 8, 128, qk["eps"], qk["q_weight"], qk["k_weight"],
+                           qk["cos_sin"], True, qk["positions"])
+    run_dsv4(ds)
+
+
+def _clone(d):
+    return {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+@pytest.mark.parametrize("large", [False, True], ids=["decode", "prefill"])
+def test_cuda_graph_capture_and_replay(cuda_device, large):
+    """Both operators recorded into one CUDA graph (several layers) and
+    replayed twice give bit-identical results to the same calls run eagerly."""
+    T_qk, T_ds = (4096, 2048) if large else (17, 16)
+    layers = [_layer_inputs(cuda_device, i, T_qk, T_ds) for i in range(4)]
+    eager = [(_clone(qk), _clone(ds)) for qk, ds in layers]
+    graphed = [(_clone(qk), _clone(ds)) for qk, ds in layers]
+    warm = [(_clone(qk), _clone(ds)) for qk, ds in layers]
+    for qk, ds in warm:  # warm-up before capture (occupancy query, lazy init)
+        _run_layer(qk, ds)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for qk, ds in eager:
+            _run_layer(qk, ds)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for qk, ds in graphed:
+            _run_layer(qk, ds)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for (qe, de), (qg, dg) in zip(eager, graphed):
+        assert torch.equal(qe["qkv"], qg["qkv"])
+        assert torch.equal(de["q"], dg["q"]) and torch.equal(de["kv_cache"], dg["kv_cache"])
