@@ -53,10 +53,12 @@
  *   - After the launch the CUDA launch error (if any) is fetched and cleared
  *     with cudaGetLastError and reported as KVQ_ERR_CUDA; the raw code is
  *     available from kvq_last_cuda_error().
- *   - Not checked (no sizes cross the ABI for them; the caller guarantees):
- *     0 <= positions[t] < rows of cos_sin_cache; slot_mapping[t] == -1 or a
- *     slot inside the cache; no two tokens map to the same slot; q/qkv do not
- *     overlap the cache.  Violations are undefined behaviour.
+ *   - Not checked by the plain entry points (no sizes cross them; the caller
+ *     guarantees): 0 <= positions[t] < rows of cos_sin_cache; slot_mapping[t]
+ *     == -1 or a slot inside the cache.  Violations are undefined behaviour;
+ *     the *_checked entry points below take the sizes and reject them.  Never
+ *     checked: no two tokens map to the same slot; q/qkv do not overlap the
+ *     cache.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -207,6 +209,40 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
  */
 kvq_status dsv4_kv_cache_gather(const uint8_t* kv_cache, int block_size, const int64_t* slots,
                                 int64_t num_rows, void* out, kvq_stream_t stream);
+
+/*
+ * Bounds-checked variants.  The entry points above cannot check positions or
+ * slots (no table or cache size crosses them); these take the sizes and a
+ * device counter, and the kernels reject what lies outside instead of
+ * reading or writing out of range:
+ *   max_pos      rows of cos_sin_cache (>= 0); a token whose position is
+ *                outside [0, max_pos) is left entirely unchanged (its q/qkv
+ *                rows are not written, no cache entry is written);
+ *   num_blocks   cache blocks (>= 0); a slot that is neither -1 nor inside
+ *                [0, num_blocks * block_size) gets no cache write (the token's
+ *                q rows are still processed) -- in the gather, a zero row;
+ *   error_count  int32 device counter, 4-byte aligned: the kernels add the
+ *                number of rejected tokens (rows, for the gather); the caller
+ *                zeroes it and reads it after the stream has run.
+ * Accepted tokens give exactly the results of the unchecked entry points.
+ * NULL or misaligned error_count, negative sizes: KVQ_ERR_NULL / _ALIGN /
+ * _SHAPE, nothing launched.  Otherwise as the unchecked entry points.
+ */
+kvq_status fused_qk_norm_rope_checked(void* qkv, int64_t num_tokens, int num_heads_q,
+                                      int num_heads_k, int num_heads_v, int head_dim,
+                                      float eps, const void* q_weight,
+                                      const void* k_weight, const float* cos_sin_cache,
+                                      int64_t max_pos, int rotary_dim, int is_neox,
+                                      const int64_t* positions, int32_t* error_count,
+                                      kvq_stream_t stream);
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache, int64_t max_pos,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int64_t num_blocks, int block_size, int32_t* error_count, kvq_stream_t stream);
+kvq_status dsv4_kv_cache_gather_checked(const uint8_t* kv_cache, int64_t num_blocks,
+                                        int block_size, const int64_t* slots, int64_t num_rows,
+                                        void* out, int32_t* error_count, kvq_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char* kvq_status_string(kvq_status status);

@@ -55,6 +55,15 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.dsv4_qnorm_rope_kv_rope_quant_insert_out.restype = _I
     L.dsv4_qnorm_rope_kv_rope_quant_insert_out.argtypes = [_P, _P, _P, _I64, _I, _F, _P, _P,
                                                            _P, _P, _P, _P, _I, _P]
+    L.fused_qk_norm_rope_checked.restype = _I
+    L.fused_qk_norm_rope_checked.argtypes = [_P, _I64, _I, _I, _I, _I, _F, _P, _P, _P, _I64, _I,
+                                             _I, _P, _P, _P]
+    L.dsv4_qnorm_rope_kv_rope_quant_insert_checked.restype = _I
+    L.dsv4_qnorm_rope_kv_rope_quant_insert_checked.argtypes = [_P, _P, _P, _I64, _I, _F, _P, _P,
+                                                               _P, _I64, _P, _P, _P, _I64, _I,
+                                                               _P, _P]
+    L.dsv4_kv_cache_gather_checked.restype = _I
+    L.dsv4_kv_cache_gather_checked.argtypes = [_P, _I64, _I, _P, _I64, _P, _P, _P]
     L.dsv4_kv_cache_gather.restype = _I
     L.dsv4_kv_cache_gather.argtypes = [_P, _I, _P, _I64, _P, _P]
     L.kvq_status_string.restype = ctypes.c_char_p
@@ -126,9 +135,13 @@ def _stream(stream, device) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _counter(errors, name="errors"):
+    return _cuda(errors, torch.int32, name)
+
+
 def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
                        q_weight, k_weight, cos_sin_cache, is_neox, positions,
-                       stream=None, rotary_dim=None) -> None:
+                       stream=None, rotary_dim=None, errors=None) -> None:
     """In-place per-head RMSNorm + RoPE of the Q and K heads of ``qkv``.
 
     qkv: bf16 [T, (Hq+Hk+Hv)*head_dim]; weights bf16 [head_dim]; cos_sin_cache
@@ -136,7 +149,9 @@ def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps
     the C entry point (stream last, default: torch's current stream).
     ``rotary_dim`` (default: the cos/sin table's width) selects partial
     rotation through ``fused_qk_norm_rope_ex``; ``is_neox`` picks NeoX (True)
-    or GPT-J (False) pairs.
+    or GPT-J (False) pairs.  ``errors`` (an int32 CUDA tensor, zeroed by the
+    caller) selects the bounds-checked launch: tokens whose position is
+    outside the table are left unchanged and counted there.
     """
     if qkv.dim() != 2 or qkv.shape[1] != (num_heads_q + num_heads_k + num_heads_v) * head_dim:
         raise ValueError("qkv must be [T, (Hq+Hk+Hv)*head_dim]")
@@ -145,23 +160,28 @@ def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps
     if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rotary_dim:
         raise ValueError("cos_sin_cache must be [max_pos, rotary_dim]")
     T = qkv.shape[0]
-    st = lib().fused_qk_norm_rope_ex(
-        _cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
-        head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
-        _cuda(k_weight, torch.bfloat16, "k_weight"),
-        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"), int(rotary_dim),
-        int(bool(is_neox)), _cuda(positions, torch.int64, "positions"),
-        _stream(stream, qkv.device))
+    args = (_cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
+            head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
+            _cuda(k_weight, torch.bfloat16, "k_weight"),
+            _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"))
+    tail = (int(rotary_dim), int(bool(is_neox)), _cuda(positions, torch.int64, "positions"))
+    if errors is None:
+        st = lib().fused_qk_norm_rope_ex(*args, *tail, _stream(stream, qkv.device))
+    else:
+        st = lib().fused_qk_norm_rope_checked(*args, cos_sin_cache.shape[0], *tail,
+                                              _counter(errors), _stream(stream, qkv.device))
     _check(st, "fused_qk_norm_rope")
 
 
 def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_sin_cache,
                                          positions, slot_mapping, kv_cache,
-                                         stream=None, q_out=None) -> None:
+                                         stream=None, q_out=None, errors=None) -> None:
     """DSV4 prologue: q [T,H,512] normalised + rotated (in place, or into
     ``q_out`` when given); the kv vectors [T,512] normalised, rotated,
     quantised and written to ``kv_cache`` uint8 [num_blocks, block_size, 584]
-    at ``slot_mapping``."""
+    at ``slot_mapping``.  ``errors`` (int32 CUDA tensor, zeroed by the caller)
+    selects the bounds-checked launch: tokens with a position outside the
+    table or a slot outside the cache are rejected and counted there."""
     if q.dim() != 3 or q.shape[2] != DSV4_DIM:
         raise ValueError("q must be [T, H, 512]")
     if kv.dim() != 2 or kv.shape[0] != q.shape[0] or kv.shape[1] != DSV4_DIM:
@@ -173,19 +193,27 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
         q_out = q
     if q_out.shape != q.shape:
         raise ValueError("q_out must have q's shape")
-    st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_out(
-        _cuda(q, torch.bfloat16, "q"), _cuda(q_out, torch.bfloat16, "q_out"),
-        _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
-        _cuda(q_weight, torch.bfloat16, "q_weight"), _cuda(kv_weight, torch.bfloat16, "kv_weight"),
-        _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"),
-        _cuda(positions, torch.int64, "positions"), _cuda(slot_mapping, torch.int64, "slot_mapping"),
-        _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1], _stream(stream, q.device))
+    head = (_cuda(q, torch.bfloat16, "q"), _cuda(q_out, torch.bfloat16, "q_out"),
+            _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
+            _cuda(q_weight, torch.bfloat16, "q_weight"),
+            _cuda(kv_weight, torch.bfloat16, "kv_weight"),
+            _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"))
+    idx = (_cuda(positions, torch.int64, "positions"),
+           _cuda(slot_mapping, torch.int64, "slot_mapping"), _cuda(kv_cache, torch.uint8, "kv_cache"))
+    if errors is None:
+        st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_out(*head, *idx, kv_cache.shape[1],
+                                                            _stream(stream, q.device))
+    else:
+        st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+            *head, cos_sin_cache.shape[0], *idx, kv_cache.shape[0], kv_cache.shape[1],
+            _counter(errors), _stream(stream, q.device))
     _check(st, "dsv4_qnorm_rope_kv_rope_quant_insert")
 
 
-def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None):
+def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None, errors=None):
     """bf16 [n, 512] rows read back from the cache entries at ``slots``
-    (int64 [n], -1 = a zero row); ``out`` is allocated if not given."""
+    (int64 [n], -1 = a zero row); ``out`` is allocated if not given.
+    ``errors`` (int32 CUDA tensor) selects the bounds-checked launch."""
     if kv_cache.dim() != 3 or kv_cache.shape[2] != ENTRY_BYTES:
         raise ValueError("kv_cache must be [num_blocks, block_size, 584]")
     n = slots.shape[0]
@@ -193,10 +221,16 @@ def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None):
         out = torch.empty((n, DSV4_DIM), dtype=torch.bfloat16, device=kv_cache.device)
     if out.shape != (n, DSV4_DIM):
         raise ValueError("out must be [len(slots), 512]")
-    st = lib().dsv4_kv_cache_gather(
-        _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1],
-        _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
-        _stream(stream, kv_cache.device))
+    if errors is None:
+        st = lib().dsv4_kv_cache_gather(
+            _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1],
+            _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
+            _stream(stream, kv_cache.device))
+    else:
+        st = lib().dsv4_kv_cache_gather_checked(
+            _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[0], kv_cache.shape[1],
+            _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
+            _counter(errors), _stream(stream, kv_cache.device))
     _check(st, "dsv4_kv_cache_gather")
     return out
 

@@ -99,14 +99,13 @@ int device_sm_count() {
 
 }  // namespace kvq
 
-extern "C" {
+namespace {
 
-kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
-                                 int num_heads_k, int num_heads_v, int head_dim,
-                                 float eps, const void* q_weight,
-                                 const void* k_weight, const float* cos_sin_cache,
-                                 int rotary_dim, int is_neox,
-                                 const int64_t* positions, kvq_stream_t stream) {
+kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads_k,
+                   int num_heads_v, int head_dim, float eps, const void* q_weight,
+                   const void* k_weight, const float* cos_sin_cache, int rotary_dim,
+                   int is_neox, const int64_t* positions, int64_t max_pos, int32_t* errors,
+                   kvq_stream_t stream) {
   if (num_tokens < 0 || num_heads_q < 0 || num_heads_k < 0 || num_heads_v < 0)
     return KVQ_ERR_SHAPE;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
@@ -136,6 +135,8 @@ kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
   a.rotary_dim = rotary_dim;
   a.is_neox = is_neox;
   a.eps = eps;
+  a.max_pos = max_pos;
+  a.errors = reinterpret_cast<int*>(errors);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (head_dim == 128 && is_neox == 1 && rotary_dim == 128)
     return finish_launch(kvq::launch_qk_norm_rope(a, qk_config_for(num_tokens, rows), st));
@@ -143,22 +144,12 @@ kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
       kvq::launch_qk_general(a, num_tokens * (int64_t)rows < kQkSmallRows, st));
 }
 
-kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
-                              int num_heads_k, int num_heads_v, int head_dim,
-                              float eps, const void* q_weight,
-                              const void* k_weight, const float* cos_sin_cache,
-                              int is_neox, const int64_t* positions,
-                              kvq_stream_t stream) {
-  return fused_qk_norm_rope_ex(qkv, num_tokens, num_heads_q, num_heads_k, num_heads_v,
-                               head_dim, eps, q_weight, k_weight, cos_sin_cache, head_dim,
-                               is_neox, positions, stream);
-}
-
-kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
-    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
-    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
-    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
-    int block_size, kvq_stream_t stream) {
+kvq_status dsv4_impl(const void* q, void* q_out, const void* kv, int64_t num_tokens,
+                     int num_heads, float eps, const void* q_weight, const void* kv_weight,
+                     const float* cos_sin_cache, const int64_t* positions,
+                     const int64_t* slot_mapping, uint8_t* kv_cache, int block_size,
+                     int64_t max_pos, int64_t num_slots, int32_t* errors,
+                     kvq_stream_t stream) {
   if (num_tokens < 0 || num_heads < 1 || block_size < 1) return KVQ_ERR_SHAPE;
   if (num_tokens * (int64_t)(num_heads + 1) >= kIndexLimit) return KVQ_ERR_SHAPE;
   if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
@@ -188,8 +179,100 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
   a.num_tokens = (int)num_tokens;
   a.num_heads = num_heads;
   a.eps = eps;
+  a.max_pos = max_pos;
+  a.num_slots = num_slots;
+  a.errors = reinterpret_cast<int*>(errors);
   return finish_launch(kvq::launch_dsv4(a, dsv4_config_for(num_tokens, num_heads),
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status gather_impl(const uint8_t* kv_cache, int block_size, const int64_t* slots,
+                       int64_t num_rows, void* out, int64_t num_slots, int32_t* errors,
+                       kvq_stream_t stream) {
+  if (num_rows < 0 || num_rows >= kIndexLimit || block_size < 1) return KVQ_ERR_SHAPE;
+  if (num_rows == 0) return KVQ_OK;
+  if (!kv_cache || !slots || !out) return KVQ_ERR_NULL;
+  if (!aligned(kv_cache, 8) || !aligned(slots, 8) || !aligned(out, 16)) return KVQ_ERR_ALIGN;
+  kvq::GatherArgs a;
+  a.kv_cache = kv_cache;
+  a.slots = slots;
+  a.out = out;
+  a.num_rows = (int)num_rows;
+  a.num_slots = num_slots;
+  a.errors = reinterpret_cast<int*>(errors);
+  return finish_launch(kvq::launch_dsv4_gather(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Extra arguments of the bounds-checked entry points.
+kvq_status check_counter(const int32_t* errors, int64_t bound) {
+  if (!errors) return KVQ_ERR_NULL;
+  if (!aligned(errors, 4)) return KVQ_ERR_ALIGN;
+  if (bound < 0) return KVQ_ERR_SHAPE;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
+                                 int num_heads_k, int num_heads_v, int head_dim,
+                                 float eps, const void* q_weight,
+                                 const void* k_weight, const float* cos_sin_cache,
+                                 int rotary_dim, int is_neox,
+                                 const int64_t* positions, kvq_stream_t stream) {
+  return qk_impl(qkv, num_tokens, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
+                 q_weight, k_weight, cos_sin_cache, rotary_dim, is_neox, positions, 0, nullptr,
+                 stream);
+}
+
+kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
+                              int num_heads_k, int num_heads_v, int head_dim,
+                              float eps, const void* q_weight,
+                              const void* k_weight, const float* cos_sin_cache,
+                              int is_neox, const int64_t* positions,
+                              kvq_stream_t stream) {
+  return qk_impl(qkv, num_tokens, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
+                 q_weight, k_weight, cos_sin_cache, head_dim, is_neox, positions, 0, nullptr,
+                 stream);
+}
+
+kvq_status fused_qk_norm_rope_checked(void* qkv, int64_t num_tokens, int num_heads_q,
+                                      int num_heads_k, int num_heads_v, int head_dim,
+                                      float eps, const void* q_weight,
+                                      const void* k_weight, const float* cos_sin_cache,
+                                      int64_t max_pos, int rotary_dim, int is_neox,
+                                      const int64_t* positions, int32_t* error_count,
+                                      kvq_stream_t stream) {
+  const kvq_status c = check_counter(error_count, max_pos);
+  if (c != KVQ_OK) return c;
+  return qk_impl(qkv, num_tokens, num_heads_q, num_heads_k, num_heads_v, head_dim, eps,
+                 q_weight, k_weight, cos_sin_cache, rotary_dim, is_neox, positions, max_pos,
+                 error_count, stream);
+}
+
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_out(
+    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int block_size, kvq_stream_t stream) {
+  return dsv4_impl(q, q_out, kv, num_tokens, num_heads, eps, q_weight, kv_weight,
+                   cos_sin_cache, positions, slot_mapping, kv_cache, block_size, 0, 0, nullptr,
+                   stream);
+}
+
+kvq_status dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+    const void* q, void* q_out, const void* kv, int64_t num_tokens, int num_heads, float eps,
+    const void* q_weight, const void* kv_weight, const float* cos_sin_cache, int64_t max_pos,
+    const int64_t* positions, const int64_t* slot_mapping, uint8_t* kv_cache,
+    int64_t num_blocks, int block_size, int32_t* error_count, kvq_stream_t stream) {
+  kvq_status c = check_counter(error_count, max_pos);
+  if (c == KVQ_OK && num_blocks < 0) c = KVQ_ERR_SHAPE;
+  if (c != KVQ_OK) return c;
+  const int64_t num_slots = block_size > 0 ? num_blocks * (int64_t)block_size : 0;
+  return dsv4_impl(q, q_out, kv, num_tokens, num_heads, eps, q_weight, kv_weight,
+                   cos_sin_cache, positions, slot_mapping, kv_cache, block_size, max_pos,
+                   num_slots, error_count, stream);
 }
 
 kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
@@ -204,16 +287,16 @@ kvq_status dsv4_qnorm_rope_kv_rope_quant_insert(
 
 kvq_status dsv4_kv_cache_gather(const uint8_t* kv_cache, int block_size, const int64_t* slots,
                                 int64_t num_rows, void* out, kvq_stream_t stream) {
-  if (num_rows < 0 || num_rows >= kIndexLimit || block_size < 1) return KVQ_ERR_SHAPE;
-  if (num_rows == 0) return KVQ_OK;
-  if (!kv_cache || !slots || !out) return KVQ_ERR_NULL;
-  if (!aligned(kv_cache, 8) || !aligned(slots, 8) || !aligned(out, 16)) return KVQ_ERR_ALIGN;
-  kvq::GatherArgs a;
-  a.kv_cache = kv_cache;
-  a.slots = slots;
-  a.out = out;
-  a.num_rows = (int)num_rows;
-  return finish_launch(kvq::launch_dsv4_gather(a, reinterpret_cast<cudaStream_t>(stream)));
+  return gather_impl(kv_cache, block_size, slots, num_rows, out, 0, nullptr, stream);
+}
+
+kvq_status dsv4_kv_cache_gather_checked(const uint8_t* kv_cache, int64_t num_blocks,
+                                        int block_size, const int64_t* slots, int64_t num_rows,
+                                        void* out, int32_t* error_count, kvq_stream_t stream) {
+  kvq_status c = check_counter(error_count, num_blocks);
+  if (c != KVQ_OK) return c;
+  const int64_t num_slots = block_size > 0 ? num_blocks * (int64_t)block_size : 0;
+  return gather_impl(kv_cache, block_size, slots, num_rows, out, num_slots, error_count, stream);
 }
 
 const char* kvq_status_string(kvq_status status) {

@@ -61,6 +61,10 @@ struct Dsv4Params {
   int q_rows;   // num_tokens * num_heads
   int kv_ctas;  // tiles kernel: leading CTAs that do KV work
   float eps;
+  // bounds-checked launches only
+  int64_t max_pos;    // rows of cos_sin
+  int64_t num_slots;  // cache capacity
+  int* errors;        // tokens rejected
 };
 
 // UE8M0 exponent byte (e + 127, clamped to [0, 254]) of the smallest power of
@@ -92,17 +96,31 @@ __device__ __forceinline__ uint2 e4m3x8(const float* v, float scale) {
 }
 
 // One row's data as held by a lane: two 16-byte chunks plus, on the rotary
-// lanes, the token's four cosines and four sines.
+// lanes, the token's four cosines and four sines; `ok` (bounds-checked
+// launches) says whether the token's position lies inside the cos/sin table.
 struct RowRegs {
   uint4 a, b;
   float4 c, s;
+  bool ok;
 };
 
+// CHECKED: every lane reads the position, so the whole warp agrees on `ok`,
+// and no cos/sin row outside the table is read.
+template <bool CHECKED>
 __device__ __forceinline__ void load_row(const Dsv4Params& p, const __nv_bfloat16* row,
                                          int64_t token, int lane, RowRegs& r) {
   r.a = load_stream(row + 8 * lane);
   r.b = load_stream(row + 256 + 8 * lane);
-  if (lane >= kRopeLane) {
+  r.ok = true;
+  if (CHECKED) {
+    const int64_t pos = __ldg(p.positions + token);
+    r.ok = pos >= 0 && pos < p.max_pos;
+    if (lane >= kRopeLane && r.ok) {
+      const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + pos * 64);
+      r.c = __ldg(cs + (lane - kRopeLane));
+      r.s = __ldg(cs + 8 + (lane - kRopeLane));
+    }
+  } else if (lane >= kRopeLane) {
     const int64_t pos = __ldg(p.positions + token);
     const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + pos * 64);
     r.c = __ldg(cs + (lane - kRopeLane));
@@ -149,8 +167,11 @@ __device__ __forceinline__ void norm_rope(const RowRegs& r, const Weights& wp, f
   }
 }
 
+// A row whose token has no valid position (checked launches) is left as is.
+template <bool CHECKED>
 __device__ __forceinline__ void q_row(const Dsv4Params& p, int row, const RowRegs& r,
                                       const Weights& w, int lane) {
+  if (CHECKED && !r.ok) return;  // warp-uniform
   float x[16];
   norm_rope(r, w, p.eps, lane, x);
   __nv_bfloat16* dst = p.q_out + (size_t)row * kDim;
@@ -167,8 +188,16 @@ __device__ __forceinline__ void store8(uint8_t* dst, uint2 v) {
   __stcs(reinterpret_cast<uint2*>(dst), v);
 }
 
+// Checked launches reject a token whose position is outside the table or
+// whose slot is neither -1 nor inside the cache: no entry is written and the
+// token is counted once (its q rows are skipped only for a bad position).
+template <bool CHECKED>
 __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, const RowRegs& r,
                                          const Weights& w, int lane) {
+  if (CHECKED && (!r.ok || slot < -1 || slot >= p.num_slots)) {  // warp-uniform
+    if (lane == 0) atomicAdd(p.errors, 1);
+    return;
+  }
   float x[16];
   norm_rope(r, w, p.eps, lane, x);
   // Block amax: chunk 0 -> blocks 0..3, chunk 1 -> blocks 4..6 (lanes < 24).
@@ -208,7 +237,7 @@ __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, cons
 
 // ---- tiles: one-shot grid -------------------------------------------------
 
-template <int WARPS, int QROWS, int MINB>
+template <int WARPS, int QROWS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_tiles_kernel(const Dsv4Params p) {
   const int lane = threadIdx.x & 31;
@@ -217,9 +246,9 @@ dsv4_tiles_kernel(const Dsv4Params p) {
     const int t = (int)blockIdx.x * WARPS + warp;
     if (t >= p.num_tokens) return;
     RowRegs r;
-    load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
+    load_row<CHECKED>(p, p.kv + (size_t)t * kDim, t, lane, r);
     const int64_t slot = __ldg(p.slot_mapping + t);
-    kv_token(p, slot, r, load_weights(p.kv_weight, lane), lane);
+    kv_token<CHECKED>(p, slot, r, load_weights(p.kv_weight, lane), lane);
     return;
   }
   const int row0 = (((int)blockIdx.x - p.kv_ctas) * WARPS + warp) * QROWS;
@@ -227,42 +256,47 @@ dsv4_tiles_kernel(const Dsv4Params p) {
 #pragma unroll
   for (int i = 0; i < QROWS; ++i)
     if (row0 + i < p.q_rows)
-      load_row(p, p.q + (size_t)(row0 + i) * kDim, (row0 + i) / p.num_heads, lane, r[i]);
+      load_row<CHECKED>(p, p.q + (size_t)(row0 + i) * kDim, (row0 + i) / p.num_heads, lane,
+                        r[i]);
   const Weights w = load_weights(p.q_weight, lane);
 #pragma unroll
   for (int i = 0; i < QROWS; ++i) {
     if (row0 + i >= p.q_rows) break;  // warp-uniform
-    q_row(p, row0 + i, r[i], w, lane);
+    q_row<CHECKED>(p, row0 + i, r[i], w, lane);
   }
 }
 
 // ---- stream: persistent grid, two-deep register pipeline ------------------
 
+template <bool CHECKED>
 __device__ __forceinline__ void stream_kv(const Dsv4Params& p, int gw, int nw, int lane) {
   if (gw >= p.num_tokens) return;
   const Weights w = load_weights(p.kv_weight, lane);
   for (int t = gw; t < p.num_tokens; t += nw) {
     RowRegs r;
-    load_row(p, p.kv + (size_t)t * kDim, t, lane, r);
-    kv_token(p, __ldg(p.slot_mapping + t), r, w, lane);
+    load_row<CHECKED>(p, p.kv + (size_t)t * kDim, t, lane, r);
+    kv_token<CHECKED>(p, __ldg(p.slot_mapping + t), r, w, lane);
   }
 }
 
+template <bool CHECKED>
 __device__ __forceinline__ void stream_q(const Dsv4Params& p, int gw, int nw, int lane) {
   int row = gw;
   if (row >= p.q_rows) return;
   const Weights w = load_weights(p.q_weight, lane);
   RowRegs r0, r1;
-  load_row(p, p.q + (size_t)row * kDim, row / p.num_heads, lane, r0);
+  load_row<CHECKED>(p, p.q + (size_t)row * kDim, row / p.num_heads, lane, r0);
   while (true) {
     int next = row + nw;
-    if (next < p.q_rows) load_row(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r1);
-    q_row(p, row, r0, w, lane);
+    if (next < p.q_rows)
+      load_row<CHECKED>(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r1);
+    q_row<CHECKED>(p, row, r0, w, lane);
     if (next >= p.q_rows) break;
     row = next;
     next = row + nw;
-    if (next < p.q_rows) load_row(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r0);
-    q_row(p, row, r1, w, lane);
+    if (next < p.q_rows)
+      load_row<CHECKED>(p, p.q + (size_t)next * kDim, next / p.num_heads, lane, r0);
+    q_row<CHECKED>(p, row, r1, w, lane);
     if (next >= p.q_rows) break;
     row = next;
   }
@@ -270,14 +304,14 @@ __device__ __forceinline__ void stream_q(const Dsv4Params& p, int gw, int nw, in
 
 // KV vectors first: each warp's share is small, and running them last was
 // measured no faster.
-template <int WARPS, int MINB>
+template <int WARPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_stream_kernel(const Dsv4Params p) {
   const int lane = threadIdx.x & 31;
   const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = (int)gridDim.x * WARPS;
-  stream_kv(p, gw, nw, lane);
-  stream_q(p, gw, nw, lane);
+  stream_kv<CHECKED>(p, gw, nw, lane);
+  stream_q<CHECKED>(p, gw, nw, lane);
 }
 
 Dsv4Params make_params(const Dsv4Args& a) {
@@ -296,30 +330,34 @@ Dsv4Params make_params(const Dsv4Args& a) {
   p.q_rows = a.num_tokens * a.num_heads;
   p.kv_ctas = 0;
   p.eps = a.eps;
+  p.max_pos = a.max_pos;
+  p.num_slots = a.num_slots;
+  p.errors = a.errors;
   return p;
 }
 
-template <int WARPS, int QROWS, int MINB>
+template <int WARPS, int QROWS, int MINB, bool CHECKED = false>
 cudaError_t launch_tiles(const Dsv4Args& a, cudaStream_t stream) {
   Dsv4Params p = make_params(a);
   p.kv_ctas = (p.num_tokens + WARPS - 1) / WARPS;
   const int q_ctas = (p.q_rows + WARPS * QROWS - 1) / (WARPS * QROWS);
-  dsv4_tiles_kernel<WARPS, QROWS, MINB><<<p.kv_ctas + q_ctas, WARPS * 32, 0, stream>>>(p);
+  dsv4_tiles_kernel<WARPS, QROWS, MINB, CHECKED>
+      <<<p.kv_ctas + q_ctas, WARPS * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int WARPS, int MINB>
+template <int WARPS, int MINB, bool CHECKED = false>
 cudaError_t launch_stream(const Dsv4Args& a, cudaStream_t stream) {
   Dsv4Params p = make_params(a);
   int per_sm = 0;
-  cudaError_t e = resident_ctas(dsv4_stream_kernel<WARPS, MINB>, WARPS * 32, &per_sm);
+  cudaError_t e = resident_ctas(dsv4_stream_kernel<WARPS, MINB, CHECKED>, WARPS * 32, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t work_warps = p.q_rows > p.num_tokens ? p.q_rows : p.num_tokens;
   int64_t grid = (int64_t)per_sm * device_sm_count();
   const int64_t need = (work_warps + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  dsv4_stream_kernel<WARPS, MINB><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
+  dsv4_stream_kernel<WARPS, MINB, CHECKED><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -332,6 +370,10 @@ const LaunchConfig kDsv4Configs[] = {
 const int kDsv4NumConfigs = sizeof(kDsv4Configs) / sizeof(kDsv4Configs[0]);
 
 cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream) {
+  if (a.errors != nullptr) {  // bounds-checked: the two dispatch shapes
+    return config == 4 ? launch_stream<8, 3, true>(a, stream)
+                       : launch_tiles<4, 1, 1, true>(a, stream);
+  }
   switch (config) {
     case 0: return launch_tiles<4, 1, 1>(a, stream);
     case 1: return launch_tiles<8, 1, 1>(a, stream);

@@ -35,6 +35,8 @@ struct GatherParams {
   const int64_t* slots;
   __nv_bfloat16* out;
   int num_rows;
+  int64_t num_slots;  // bounds-checked launches: cache capacity
+  int* errors;        // bounds-checked launches: rows rejected
 };
 
 // 2^(byte - 127) as a binary32 (byte 0 gives the subnormal 2^-127).
@@ -57,6 +59,9 @@ __device__ __forceinline__ uint4 dequant8(const uint2 codes, float scale) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Checked launches turn a slot that is neither -1 nor inside the cache into a
+// zero row and count it.
+template <bool CHECKED>
 __global__ void __launch_bounds__(kWarps * 32)
 dsv4_gather_kernel(const GatherParams p) {
   const int lane = threadIdx.x & 31;
@@ -64,7 +69,9 @@ dsv4_gather_kernel(const GatherParams p) {
   if (row >= p.num_rows) return;  // whole warp leaves together
   __nv_bfloat16* dst = p.out + (size_t)row * kDim;
   const int64_t slot = __ldg(p.slots + row);
-  if (slot < 0) {
+  const bool bad = CHECKED && (slot < -1 || slot >= p.num_slots);
+  if (bad && lane == 0) atomicAdd(p.errors, 1);
+  if (slot < 0 || bad) {
     store_stream(dst + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
     store_stream(dst + 256 + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
     return;
@@ -100,8 +107,11 @@ cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream) {
   p.slots = a.slots;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.num_rows = a.num_rows;
+  p.num_slots = a.num_slots;
+  p.errors = a.errors;
   const unsigned grid = (unsigned)((p.num_rows + kWarps - 1) / kWarps);
-  dsv4_gather_kernel<<<grid, kWarps * 32, 0, stream>>>(p);
+  if (a.errors != nullptr) dsv4_gather_kernel<true><<<grid, kWarps * 32, 0, stream>>>(p);
+  else dsv4_gather_kernel<false><<<grid, kWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

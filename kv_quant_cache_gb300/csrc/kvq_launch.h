@@ -19,6 +19,9 @@ struct QkArgs {
   int num_heads_q, num_heads_k, num_heads_v;
   int head_dim, rotary_dim, is_neox;
   float eps;
+  // bounds-checked launches (errors != nullptr): rows of cos_sin
+  int64_t max_pos = 0;
+  int* errors = nullptr;
 };
 
 struct Dsv4Args {
@@ -34,6 +37,9 @@ struct Dsv4Args {
   int num_tokens;
   int num_heads;
   float eps;
+  // bounds-checked launches (errors != nullptr): rows of cos_sin, cache slots
+  int64_t max_pos = 0, num_slots = 0;
+  int* errors = nullptr;
 };
 
 struct GatherArgs {
@@ -41,6 +47,9 @@ struct GatherArgs {
   const int64_t* slots;
   void* out;
   int num_rows;
+  // bounds-checked launches (errors != nullptr): cache slots
+  int64_t num_slots = 0;
+  int* errors = nullptr;
 };
 
 // A launch shape of one operator (an instantiation of one of its kernels).

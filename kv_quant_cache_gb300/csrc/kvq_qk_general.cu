@@ -42,6 +42,8 @@ struct GenParams {
   int rot;
   int chunks, steps, items;
   float eps;
+  int64_t max_pos;  // bounds-checked launches: rows of cos_sin
+  int* errors;      // bounds-checked launches: tokens rejected
 };
 
 __device__ __forceinline__ void unpack4(const uint2& v, float* f) {
@@ -72,7 +74,7 @@ __device__ __forceinline__ void fragment_offsets(int l, int rot, int& a, int& b)
   }
 }
 
-template <int D, int STEPS, bool NEOX>
+template <int D, int STEPS, bool NEOX, bool CHECKED>
 __global__ void __launch_bounds__(128)
 qk_general_kernel(const GenParams p) {
   constexpr int LPR = D / 8;     // lanes per row
@@ -103,6 +105,15 @@ qk_general_kernel(const GenParams p) {
     }
   }
 
+  // Checked launches: a token whose position is outside the table keeps its
+  // rows unchanged and is counted once, by the item holding its first chunk.
+  if (CHECKED) {
+    const int64_t pos = __ldg(p.positions + t);
+    if (pos < 0 || pos >= p.max_pos) {  // warp-uniform
+      if (c == 0 && lane == 0) atomicAdd(p.errors, 1);
+      return;
+    }
+  }
   // Cosines and sines of the lane's four pairs: frequency 4l + k.
   float cs[4] = {0.f, 0.f, 0.f, 0.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
   if (rot_lane) {
@@ -168,7 +179,7 @@ qk_general_kernel(const GenParams p) {
   }
 }
 
-template <int D, int STEPS, bool NEOX>
+template <int D, int STEPS, bool NEOX, bool CHECKED>
 cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
   constexpr int RPW = 32 / (D / 8);
   GenParams p;
@@ -182,12 +193,14 @@ cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
   p.row_elems = (int64_t)(p.num_rows + a.num_heads_v) * D;
   p.rot = a.rotary_dim;
   p.eps = a.eps;
+  p.max_pos = a.max_pos;
+  p.errors = a.errors;
   const int groups = (p.num_rows + RPW - 1) / RPW;  // row groups of one warp step
   p.chunks = (groups + STEPS - 1) / STEPS;
   p.steps = (groups + p.chunks - 1) / p.chunks;
   p.items = a.num_tokens * p.chunks;
   const unsigned grid = (unsigned)((p.items + 3) / 4);
-  qk_general_kernel<D, STEPS, NEOX><<<grid, 128, 0, stream>>>(p);
+  qk_general_kernel<D, STEPS, NEOX, CHECKED><<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -195,10 +208,17 @@ cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
 // length.  (Six steps for head_dim 64, which would split 40 rows into two
 // equal chunks, measured no faster: the extra registers cost the occupancy
 // the balancing gained.)
+template <int D, int BIG, bool CHECKED>
+cudaError_t launch_c(const QkArgs& a, bool small, cudaStream_t stream) {
+  if (a.is_neox)
+    return small ? launch<D, 1, true, CHECKED>(a, stream) : launch<D, BIG, true, CHECKED>(a, stream);
+  return small ? launch<D, 1, false, CHECKED>(a, stream) : launch<D, BIG, false, CHECKED>(a, stream);
+}
+
 template <int D, int BIG>
 cudaError_t launch_d(const QkArgs& a, bool small, cudaStream_t stream) {
-  if (a.is_neox) return small ? launch<D, 1, true>(a, stream) : launch<D, BIG, true>(a, stream);
-  return small ? launch<D, 1, false>(a, stream) : launch<D, BIG, false>(a, stream);
+  return a.errors != nullptr ? launch_c<D, BIG, true>(a, small, stream)
+                             : launch_c<D, BIG, false>(a, small, stream);
 }
 
 }  // namespace

@@ -50,6 +50,8 @@ struct QkParams {
   int steps;          // row pairs per chunk (<= the kernel's STEPS)
   int items;          // num_tokens * chunks
   float eps;
+  int64_t max_pos;    // bounds-checked launches: rows of cos_sin
+  int* errors;        // bounds-checked launches: tokens rejected
 };
 
 // Weight fragments of this lane (dims [4l, 4l+4) and [64+4l, 64+4l+4), Q and
@@ -118,6 +120,7 @@ template <int STEPS>
 struct ItemRegs {
   uint2 lo[STEPS], hi[STEPS];
   float4 c, s;
+  bool ok;  // bounds-checked launches: the position lies inside the table
 };
 
 // Work item `item` = (token t, chunk c of row pairs).  Lanes 0-15 take rows
@@ -135,7 +138,7 @@ __device__ __forceinline__ ItemPos item_pos(const QkParams& p, int item, int hal
   return ip;
 }
 
-template <int STEPS>
+template <int STEPS, bool CHECKED>
 __device__ __forceinline__ void load_item(const QkParams& p, const ItemPos& ip, int l16,
                                           ItemRegs<STEPS>& r) {
   const __nv_bfloat16* tok = p.qkv + (size_t)ip.t * (size_t)p.row_elems;
@@ -149,12 +152,24 @@ __device__ __forceinline__ void load_item(const QkParams& p, const ItemPos& ip, 
       r.hi[s] = __ldcs(row + 16 + l16);
     }
   }
+  r.ok = true;
+  if (CHECKED) {  // no cos/sin row outside the table is read
+    const int64_t pos = __ldg(p.positions + ip.t);
+    r.ok = pos >= 0 && pos < p.max_pos;
+    if (!r.ok) return;
+  }
   load_cos_sin(p, ip.t, l16, r.c, r.s);
 }
 
-template <int STEPS>
+// A token whose position is outside the table (checked launches) keeps its
+// rows unchanged and is counted once, by the item holding its first chunk.
+template <int STEPS, bool CHECKED>
 __device__ __forceinline__ void compute_item(const QkParams& p, const ItemPos& ip, int half,
                                              int l16, const QkWeights& w, ItemRegs<STEPS>& r) {
+  if (CHECKED && !r.ok) {  // warp-uniform
+    if (ip.first == 0 && l16 == 0) atomicAdd(p.errors, 1);
+    return;
+  }
   __nv_bfloat16* tok = p.qkv + (size_t)ip.t * (size_t)p.row_elems;
 #pragma unroll
   for (int s = 0; s < STEPS; ++s) {
@@ -169,16 +184,16 @@ __device__ __forceinline__ void compute_item(const QkParams& p, const ItemPos& i
   }
 }
 
-template <int STEPS>
+template <int STEPS, bool CHECKED = false>
 __device__ __forceinline__ void do_item(const QkParams& p, int item, int half, int l16,
                                         const QkWeights& w) {
   const ItemPos ip = item_pos(p, item, half);
   ItemRegs<STEPS> r;
-  load_item<STEPS>(p, ip, l16, r);
-  compute_item<STEPS>(p, ip, half, l16, w, r);
+  load_item<STEPS, CHECKED>(p, ip, l16, r);
+  compute_item<STEPS, CHECKED>(p, ip, half, l16, w, r);
 }
 
-template <int WARPS, int STEPS, int MINB>
+template <int WARPS, int STEPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 qk_tiles_kernel(const QkParams p) {
   const int lane = threadIdx.x & 31;
@@ -186,7 +201,7 @@ qk_tiles_kernel(const QkParams p) {
   if (item >= p.items) return;  // whole warp leaves together
   QkWeights w;
   load_weights(p, lane & 15, w);
-  do_item<STEPS>(p, item, lane >> 4, lane & 15, w);
+  do_item<STEPS, CHECKED>(p, item, lane >> 4, lane & 15, w);
 }
 
 template <int WARPS, int STEPS, int MINB>
@@ -218,14 +233,16 @@ QkParams make_params(const QkArgs& a, int steps) {
   p.steps = (pairs + p.chunks - 1) / p.chunks;
   p.items = p.num_tokens * p.chunks;
   p.eps = a.eps;
+  p.max_pos = a.max_pos;
+  p.errors = a.errors;
   return p;
 }
 
-template <int WARPS, int STEPS, int MINB>
+template <int WARPS, int STEPS, int MINB, bool CHECKED = false>
 cudaError_t launch_tiles(const QkArgs& a, cudaStream_t stream) {
   const QkParams p = make_params(a, STEPS);
   const unsigned grid = (unsigned)((p.items + WARPS - 1) / WARPS);
-  qk_tiles_kernel<WARPS, STEPS, MINB><<<grid, WARPS * 32, 0, stream>>>(p);
+  qk_tiles_kernel<WARPS, STEPS, MINB, CHECKED><<<grid, WARPS * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -257,6 +274,10 @@ const LaunchConfig kQkConfigs[] = {
 const int kQkNumConfigs = sizeof(kQkConfigs) / sizeof(kQkConfigs[0]);
 
 cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream) {
+  if (a.errors != nullptr) {  // bounds-checked: the two dispatch shapes
+    return config == 2 ? launch_tiles<4, 4, 1, true>(a, stream)
+                       : launch_tiles<4, 1, 1, true>(a, stream);
+  }
   switch (config) {
     case 0: return launch_tiles<4, 1, 1>(a, stream);
     case 1: return launch_tiles<8, 2, 1>(a, stream);

@@ -228,3 +228,26 @@ def test_out_of_place_validation(L):
     assert o(q_out=A16 + 1024) == kvq.KVQ_ERR_VALUE          # partial overlap
     assert o(q_out=A16 - 4096) == kvq.KVQ_ERR_VALUE
     assert o(T=0, q=None, q_out=None) == kvq.KVQ_OK
+
+
+def test_checked_entry_points_validation(L):
+    # every call below fails validation before any launch (fake addresses)
+    E = A16 + 2**20
+    args_qk = (A16, 4, 2, 1, 1, 128, 1e-6, A16, A16, A16)
+    assert L.fused_qk_norm_rope_checked(*args_qk, 64, 128, 1, A16, None, None) == kvq.KVQ_ERR_NULL
+    assert L.fused_qk_norm_rope_checked(*args_qk, 64, 128, 1, A16, E + 2, None) == kvq.KVQ_ERR_ALIGN
+    assert L.fused_qk_norm_rope_checked(*args_qk, -1, 128, 1, A16, E, None) == kvq.KVQ_ERR_SHAPE
+    assert L.fused_qk_norm_rope_checked(A16, 4, 2, 1, 1, 96, 1e-6, A16, A16, A16, 64, 96, 1, A16,
+                                        E, None) == kvq.KVQ_ERR_UNSUPPORTED
+    head = (A16, A16, A16, 4, 2, 1e-6, A16, A16, A16)
+    assert L.dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+        *head, 64, A16, A16, A16, 8, 64, None, None) == kvq.KVQ_ERR_NULL
+    assert L.dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+        *head, 64, A16, A16, A16, -1, 64, E, None) == kvq.KVQ_ERR_SHAPE
+    assert L.dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+        *head, -5, A16, A16, A16, 8, 64, E, None) == kvq.KVQ_ERR_SHAPE
+    assert L.dsv4_qnorm_rope_kv_rope_quant_insert_checked(
+        *head, 64, A16, A16, A16, 8, 64, E + 1, None) == kvq.KVQ_ERR_ALIGN
+    assert L.dsv4_kv_cache_gather_checked(A16, 8, 64, A16, 4, A16, None, None) == kvq.KVQ_ERR_NULL
+    assert L.dsv4_kv_cache_gather_checked(A16, -1, 64, A16, 4, A16, E, None) == kvq.KVQ_ERR_SHAPE
+    assert L.dsv4_kv_cache_gather_checked(A16, 8, 64, A16, 4, A16 + 8, E, None) == kvq.KVQ_ERR_ALIGN
