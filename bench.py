@@ -554,8 +554,12 @@ def sweep(kvq, device):
         d = wl.make_qk_workload(w, device=device)
         run_configs("qk", w.name, qk_bytes(w.T, w.Hq, w.Hk), lambda: launch_qk(kvq, d, stream), 30)
         del d
-    # the general QK kernel (head_dim 64/256, GPT-J pairs, partial rotation)
+    # the general QK kernel (head_dim 64/256, GPT-J pairs, partial rotation):
+    # the automatic choice and both fragment widths forced
+    general = [(i, n) for i, n in enumerate(kvq.configs("qk")) if n.startswith("general")]
     for (T, hq, hk, hv, D, rot, neox) in ((32768, 32, 8, 8, 64, 64, True),
+                                          (32768, 32, 8, 8, 64, 32, False),
+                                          (32768, 32, 8, 8, 128, 64, True),
                                           (32768, 32, 8, 8, 128, 64, False),
                                           (32768, 32, 8, 8, 128, 128, False),
                                           (16384, 32, 8, 8, 256, 256, True),
@@ -570,11 +574,16 @@ def sweep(kvq, device):
             kvq.fused_qk_norm_rope(d["qkv"], hq, hk, hv, D, d["eps"], d["q_weight"],
                                    d["k_weight"], d["cos_sin"], neox, d["positions"],
                                    stream=stream, rotary_dim=rot)
-        med, _ = _time_launch(fn, 30, stream, flush if small else None)
-        emit({"sweep": f"qk_T{T}_{hq}-{hk}-{hv}_D{D}_rot{rot}_{'neox' if neox else 'gptj'}",
-              "config": "general", "bytes": nb, "us_median": round(med * 1e3, 2),
-              "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
-              "l2_flush": small})
+        for cid, cname in [(-1, "auto")] + general:
+            old = kvq.set_config("qk", cid)
+            try:
+                med, _ = _time_launch(fn, 30, stream, flush if small else None)
+            finally:
+                kvq.set_config("qk", old)
+            emit({"sweep": f"qk_T{T}_{hq}-{hk}-{hv}_D{D}_rot{rot}_{'neox' if neox else 'gptj'}",
+                  "config": cname, "bytes": nb, "us_median": round(med * 1e3, 2),
+                  "gbs": round(nb / med / 1e6, 1),
+                  "pct_peak": round(100 * nb / med / 1e6 / peak, 1), "l2_flush": small})
         del d
     for w in [wl.DSV4_DECODE, wl.DSV4_LARGE, *wl.DSV4_SWEEP]:
         d = wl.make_dsv4_workload(w, device=device)

@@ -266,10 +266,15 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
 
 /*
  * Launch shapes (diagnostics and tuning).  Each operator has a fixed table of
- * launch configurations (kernel shape, warps per CTA, rows per warp); every
- * configuration computes bit-identical results.  The automatic dispatch picks
- * one by problem size; the override forces one for every later call of the
- * process (benchmark sweeps, tests).
+ * launch configurations (kernel shape, warps per CTA, rows per warp).  The
+ * automatic dispatch picks one by problem size; the override forces one for
+ * every later call of the process (benchmark sweeps, tests).  Every DSV4
+ * configuration computes bit-identical results.  QK configurations 0-4 are
+ * launch shapes of the head_dim-128 full-NeoX kernel and agree bit for bit;
+ * layouts other than that one take the general kernel with 4-dim fragments.
+ * QK configurations 5 and 6 force the general kernel, with 4- or 8-dim
+ * fragments, for every layout; its sum of squares is added in another order,
+ * so it agrees with 0-4 within the operator's rounding, not bit for bit.
  *   *_num_configs   number of configurations
  *   *_config_name   static name of configuration id (NULL if out of range)
  *   kvq_set_*_config  force id (0 <= id < num) or restore automatic (id < 0);

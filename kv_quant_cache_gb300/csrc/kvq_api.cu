@@ -21,6 +21,12 @@ constexpr int kDsv4SmallConfig = 0;  // tiles<4w,1row>
 constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg>
 constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
 constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
+// Entries of kQkConfigs that name the general kernel (any layout) with 4- or
+// 8-dim fragments; forcing one routes every layout through that kernel.
+constexpr int kQkGeneralFrag4Config = 5;
+constexpr int kQkGeneralFrag8Config = 6;
+// Fragment width the general kernel takes for layouts outside the tuned one.
+constexpr int kQkGeneralFrag = 4;
 // Q+K head rows below which the QK operator takes its small-batch shape.
 constexpr int64_t kQkSmallRows = 152 * 8;
 
@@ -138,10 +144,14 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   a.max_pos = max_pos;
   a.errors = reinterpret_cast<int*>(errors);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool small = num_tokens * (int64_t)rows < kQkSmallRows;
+  const int config = qk_config_for(num_tokens, rows);
+  if (config == kQkGeneralFrag4Config || config == kQkGeneralFrag8Config)
+    return finish_launch(
+        kvq::launch_qk_general(a, small, config == kQkGeneralFrag8Config ? 8 : 4, st));
   if (head_dim == 128 && is_neox == 1 && rotary_dim == 128)
-    return finish_launch(kvq::launch_qk_norm_rope(a, qk_config_for(num_tokens, rows), st));
-  return finish_launch(
-      kvq::launch_qk_general(a, num_tokens * (int64_t)rows < kQkSmallRows, st));
+    return finish_launch(kvq::launch_qk_norm_rope(a, config, st));
+  return finish_launch(kvq::launch_qk_general(a, small, kQkGeneralFrag, st));
 }
 
 kvq_status dsv4_impl(const void* q, void* q_out, const void* kv, int64_t num_tokens,

@@ -64,8 +64,9 @@ extern const int kDsv4NumConfigs;
 
 // Tuned kernel: head_dim 128, full-dimension NeoX rotation.
 cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream);
-// Every other supported layout (head_dim 64/128/256, NeoX or GPT-J, partial).
-cudaError_t launch_qk_general(const QkArgs& a, bool small, cudaStream_t stream);
+// Every supported layout (head_dim 64/128/256, NeoX or GPT-J, partial), with
+// fragments of frag = 4 or 8 dims per lane.
+cudaError_t launch_qk_general(const QkArgs& a, bool small, int frag, cudaStream_t stream);
 cudaError_t launch_dsv4(const Dsv4Args& a, int config, cudaStream_t stream);
 cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream);
 

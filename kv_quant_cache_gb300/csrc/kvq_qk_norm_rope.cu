@@ -269,7 +269,7 @@ cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
 
 const LaunchConfig kQkConfigs[] = {
     {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"}, {"tiles<8w,4step>"},
-    {"stream<8w,4step>"},
+    {"stream<8w,4step>"}, {"general<frag4>"}, {"general<frag8>"},
 };
 const int kQkNumConfigs = sizeof(kQkConfigs) / sizeof(kQkConfigs[0]);
 

@@ -84,7 +84,7 @@ def test_runs_on_a_side_stream(cuda_device):
     assert torch.equal(d["qkv"], ref["qkv"])
 
 
-QK_CONFIGS = list(range(5))
+QK_CONFIGS = list(range(7))
 
 
 @pytest.mark.parametrize("config", QK_CONFIGS)
@@ -103,16 +103,20 @@ LAYOUTS = [(D, rot, neox) for D in (64, 128, 256) for neox in (True, False)
            for rot in sorted({16, D // 2, D}) if rot % 16 == 0 and not (D == 128 and rot == 128 and neox)]
 
 
+@pytest.mark.parametrize("config", [-1, 5, 6], ids=["auto", "frag4", "frag8"])
 @pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: f"D{l[0]}_rot{l[1]}_{'neox' if l[2] else 'gptj'}")
 @pytest.mark.parametrize("shape", [(1, 4, 2, 1), (17, 3, 1, 2), (777, 8, 2, 2), (300, 0, 5, 0)])
-def test_general_layouts(cuda_device, layout, shape):
+def test_general_layouts(cuda_device, layout, shape, config):
     """head_dim 64/128/256, NeoX or GPT-J pairs, full or partial rotation,
-    through the general kernel, against the oracle."""
+    through the general kernel (automatic choice, then 4- and 8-dim fragments
+    forced), against the oracle."""
+    assert kvq.configs("qk")[5:] == ["general<frag4>", "general<frag8>"]
     D, rot, neox = layout
     T, Hq, Hk, Hv = shape
     d = wl.make_qk(T, Hq, Hk, Hv, D=D, theta=1e4, max_pos=8192, seed=D + rot + T,
                    device=cuda_device, rotary_dim=rot, is_neox=neox)
-    qk_parity(d)
+    with with_config("qk", config):
+        qk_parity(d)
 
 
 def test_general_layout_at_scale(cuda_device):
