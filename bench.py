@@ -518,8 +518,8 @@ def _time_launch(fn, reps, stream, flush=None):
 
 def sweep(kvq, device):
     """Every workload under every launch configuration, the DSV4 dispatch
-    crossover, and a 512 MiB device-to-device copy ceiling (JSON lines on
-    stderr)."""
+    crossover, a 512 MiB device-to-device copy ceiling and the pinned-host
+    link's copy ceiling (JSON lines on stderr)."""
     peak, _ = peak_hbm()
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
@@ -536,6 +536,28 @@ def sweep(kvq, device):
     emit({"sweep": "d2d_copy_512MiB", "gbs_median": round(2 * src.numel() / med / 1e6, 1),
           "gbs_best": round(2 * src.numel() / best / 1e6, 1)})
     del src, dst
+    # host-link ceiling for the end-to-end figures: 1 GiB pinned host <-> HBM
+    # copies, each direction alone, then both at once on two streams
+    h_in = torch.empty(2**30, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(2**30, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(2**30, dtype=torch.uint8, device=device)
+    d_out = torch.empty(2**30, dtype=torch.uint8, device=device)
+    side = torch.cuda.Stream(device)
+
+    def both():
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            h_out.copy_(d_out, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        stream.wait_stream(side)
+    with torch.cuda.stream(stream):
+        t_h2d, _ = _time_launch(lambda: d_in.copy_(h_in, non_blocking=True), 5, stream)
+        t_d2h, _ = _time_launch(lambda: h_out.copy_(d_out, non_blocking=True), 5, stream)
+        t_both, _ = _time_launch(both, 5, stream)
+    emit({"sweep": "host_link_1GiB", "h2d_gbs": round(2**30 / t_h2d / 1e6, 1),
+          "d2h_gbs": round(2**30 / t_d2h / 1e6, 1),
+          "both_gbs": round(2 * 2**30 / t_both / 1e6, 1)})
+    del h_in, h_out, d_in, d_out
 
     def run_configs(op, name, nb, fn, reps):
         small = nb < 256 * 2**20
