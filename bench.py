@@ -572,10 +572,41 @@ def sweep(kvq, device):
                   "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1),
                   "l2_flush": small})
 
-    for w in (wl.QK_SMALL, wl.QK_LARGE):
+    for w in (wl.QK_SMALL, wl.QK_LARGE,
+              wl.QKWorkload("qk_T131072_32-8-8", T=131072, Hq=32, Hk=8, Hv=8, theta=1e6,
+                            max_pos=131072, seed=1001)):
         d = wl.make_qk_workload(w, device=device)
         run_configs("qk", w.name, qk_bytes(w.T, w.Hq, w.Hk), lambda: launch_qk(kvq, d, stream), 30)
         del d
+    # QK launch-shape crossover: the small-batch, register-pipelined and
+    # TMA-staged shapes of the head_dim-128 kernel over the token count
+    names = kvq.configs("qk")
+    cand = [names.index(n) for n in ("tiles<4w,1step>", "tiles<4w,4step>") if n in names]
+    cand += [i for i, n in enumerate(names) if n.startswith("bulk")]
+    for T in (1, 16, 64, 256, 1024, 2048, 4096, 8192, 16384, 65536):
+        d = wl.make_qk(T, 32, 8, 8, theta=1e6, max_pos=131072, seed=5 + T, device=device)
+        nb = qk_bytes(T, 32, 8)
+        small = nb < 256 * 2**20
+        res = {}
+        for cid in cand:
+            old = kvq.set_config("qk", cid)
+            try:
+                res[names[cid]] = round(_time_launch(lambda: launch_qk(kvq, d, stream), 30, stream,
+                                                     flush if small else None)[0] * 1e3, 2)
+            finally:
+                kvq.set_config("qk", old)
+        emit({"sweep": "qk_dispatch", "T": T, "rows": T * 40, "bytes": nb, "us": res,
+              "auto": names[kvq.qk_config_for(T, 32, 8)]})
+        del d
+    # a copy moving the QK step's bytes (Q+K rows read and written): the
+    # ceiling for a launch of that length
+    nb = qk_bytes(wl.QK_LARGE.T, wl.QK_LARGE.Hq, wl.QK_LARGE.Hk)
+    src = torch.empty(nb // 2, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    med, _ = _time_launch(lambda: dst.copy_(src), 30, stream)
+    emit({"sweep": "d2d_copy_qk_T32768_bytes", "bytes": nb, "us_median": round(med * 1e3, 2),
+          "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1)})
+    del src, dst
     # the general QK kernel (head_dim 64/256, GPT-J pairs, partial rotation):
     # the automatic choice and both fragment widths forced
     general = [(i, n) for i, n in enumerate(kvq.configs("qk")) if n.startswith("general")]

@@ -269,12 +269,14 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * launch configurations (kernel shape, warps per CTA, rows per warp).  The
  * automatic dispatch picks one by problem size; the override forces one for
  * every later call of the process (benchmark sweeps, tests).  Every DSV4
- * configuration computes bit-identical results.  QK configurations 0-4 are
- * launch shapes of the head_dim-128 full-NeoX kernel and agree bit for bit;
- * layouts other than that one take the general kernel with 4-dim fragments.
- * QK configurations 5 and 6 force the general kernel, with 4- or 8-dim
+ * configuration computes bit-identical results.  QK configurations 0-4
+ * (register-pipelined) and 7-9 (TMA-staged, bulk<...>) are launch shapes of
+ * the head_dim-128 full-NeoX kernels and agree bit for bit; layouts other
+ * than that one take the general kernel with 4-dim fragments.  QK
+ * configurations 5 and 6 force the general kernel, with 4- or 8-dim
  * fragments, for every layout; its sum of squares is added in another order,
- * so it agrees with 0-4 within the operator's rounding, not bit for bit.
+ * so it agrees with the others within the operator's rounding, not bit for
+ * bit.
  *   *_num_configs   number of configurations
  *   *_config_name   static name of configuration id (NULL if out of range)
  *   kvq_set_*_config  force id (0 <= id < num) or restore automatic (id < 0);
@@ -283,6 +285,22 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  *                   launches on other threads.
  *   *_config_for    the configuration a call with these sizes would use now
  */
+/*
+ * Staged QK launch shapes (configurations named bulk<...>): each warp keeps
+ * its next items in flight in shared memory through the bulk-copy (TMA)
+ * engine and waits on an mbarrier per stage.  Every such wait polls at most
+ * `polls` times (default 1 << 22) and for at most 20 ms.  A warp whose wait
+ * runs out lets its copies in flight land (each wait bounded again), then
+ * finishes its remaining rows from global memory, with the same results: the
+ * limit bounds how long a stalled copy can hold a warp and never changes an
+ * output.  0 sends every staged launch straight to that path (diagnostics and
+ * tests).  Applies to launches enqueued after the call; returns the previous
+ * limit.  Not synchronised with launches on other threads.  The staged shapes
+ * serve only qkv and cos/sin tables in device memory; other buffers take the
+ * register-pipelined large-batch shape.
+ */
+uint32_t kvq_set_qk_stage_wait_limit(uint32_t polls);
+
 int kvq_qk_num_configs(void);
 const char* kvq_qk_config_name(int id);
 int kvq_set_qk_config(int id);

@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libkvq.so")
 
-SOURCES = ["kvq_api.cu", "kvq_qk_norm_rope.cu", "kvq_qk_general.cu", "kvq_dsv4.cu",
-           "kvq_dsv4_gather.cu"]
+SOURCES = ["kvq_api.cu", "kvq_qk_norm_rope.cu", "kvq_qk_bulk.cu", "kvq_qk_general.cu",
+           "kvq_dsv4.cu", "kvq_dsv4_gather.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE, "-I", CSRC]

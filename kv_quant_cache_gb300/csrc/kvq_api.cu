@@ -7,6 +7,7 @@
 
 #include "kvq.h"
 #include "kvq_launch.h"
+#include "kvq_qk_bulk.h"
 
 namespace {
 
@@ -21,14 +22,19 @@ constexpr int kDsv4SmallConfig = 0;  // tiles<4w,1row>
 constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg>
 constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
 constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
+constexpr int kQkStagedConfig = 8;   // bulk<24w,2st,12r>
 // Entries of kQkConfigs that name the general kernel (any layout) with 4- or
 // 8-dim fragments; forcing one routes every layout through that kernel.
 constexpr int kQkGeneralFrag4Config = 5;
 constexpr int kQkGeneralFrag8Config = 6;
 // Fragment width the general kernel takes for layouts outside the tuned one.
 constexpr int kQkGeneralFrag = 4;
-// Q+K head rows below which the QK operator takes its small-batch shape.
+// Q+K head rows below which the QK operator takes its small-batch shape, and
+// from which it takes the TMA-staged shape (measured on GB300 by the
+// benchmark's QK crossover sweep: the staged shape ties the register-pipelined
+// one near 80K rows and wins from 160K rows on, by 6-11 % at 2.6M-5.2M rows).
 constexpr int64_t kQkSmallRows = 152 * 8;
+constexpr int64_t kQkStagedRows = 131072;
 
 std::atomic<int64_t> g_threshold{-1};
 std::atomic<int> g_dsv4_config{-1};
@@ -68,7 +74,8 @@ constexpr int64_t kIndexLimit = (int64_t)1 << 31;
 int qk_config_for(int64_t num_tokens, int rows) {
   const int forced = g_qk_config.load(std::memory_order_relaxed);
   if (forced >= 0) return forced;
-  return num_tokens * (int64_t)rows < kQkSmallRows ? kQkSmallConfig : kQkLargeConfig;
+  const int64_t n = num_tokens * (int64_t)rows;
+  return n < kQkSmallRows ? kQkSmallConfig : n < kQkStagedRows ? kQkLargeConfig : kQkStagedConfig;
 }
 
 int dsv4_config_for(int64_t num_tokens, int num_heads) {
@@ -335,6 +342,8 @@ int64_t kvq_set_dsv4_dispatch_threshold(int64_t value) {
 int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
   return num_tokens * (int64_t)(num_heads + 1) < current_threshold() ? 0 : 1;
 }
+
+uint32_t kvq_set_qk_stage_wait_limit(uint32_t polls) { return kvq::set_qk_stage_wait_limit(polls); }
 
 int kvq_qk_num_configs(void) { return kvq::kQkNumConfigs; }
 

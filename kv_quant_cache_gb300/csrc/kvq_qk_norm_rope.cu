@@ -29,12 +29,16 @@
 // kept: at 74-86 registers it holds too few warps.)
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
+#include "kvq_qk_bulk.h"
+#include "kvq_qk_row.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int kHeadDim = 128;
-constexpr int kHalf = kHeadDim / 2;
+using qk128::kHalf;
+using qk128::kHeadDim;
+using qk128::row_math;
+using QkWeights = qk128::Weights;
 
 struct QkParams {
   __nv_bfloat16* qkv;
@@ -54,28 +58,6 @@ struct QkParams {
   int* errors;        // bounds-checked launches: tokens rejected
 };
 
-// Weight fragments of this lane (dims [4l, 4l+4) and [64+4l, 64+4l+4), Q and
-// K), kept packed as bf16 and widened where they are used.
-struct QkWeights {
-  uint2 q_lo, q_hi, k_lo, k_hi;
-};
-
-__device__ __forceinline__ void load_weights(const QkParams& p, int l16, QkWeights& w) {
-  const uint2* q = reinterpret_cast<const uint2*>(p.q_weight);
-  const uint2* k = reinterpret_cast<const uint2*>(p.k_weight);
-  w.q_lo = __ldg(q + l16);
-  w.q_hi = __ldg(q + 16 + l16);
-  w.k_lo = __ldg(k + l16);
-  w.k_hi = __ldg(k + 16 + l16);
-}
-
-__device__ __forceinline__ void unpack_bf16x4(const uint2& v, float* f) {
-  f[0] = __uint_as_float(v.x << 16);
-  f[1] = __uint_as_float(v.x & 0xffff0000u);
-  f[2] = __uint_as_float(v.y << 16);
-  f[3] = __uint_as_float(v.y & 0xffff0000u);
-}
-
 // The lane's 4 cosines and 4 sines of the token's row.
 __device__ __forceinline__ void load_cos_sin(const QkParams& p, int t, int l16, float4& c,
                                              float4& s) {
@@ -83,35 +65,6 @@ __device__ __forceinline__ void load_cos_sin(const QkParams& p, int t, int l16, 
   const float4* crow = reinterpret_cast<const float4*>(p.cos_sin + pos * kHeadDim);
   c = __ldg(crow + l16);
   s = __ldg(crow + kHalf / 4 + l16);
-}
-
-// Normalise + rotate one row fragment; all 32 lanes must call it together
-// (the sum of squares is reduced across the half-warp).
-__device__ __forceinline__ void row_math(uint2& lo, uint2& hi, bool is_q, const QkWeights& w,
-                                         const float4& c4, const float4& s4, float eps) {
-  float a[4], b[4];
-  unpack_bf16x4(lo, a);
-  unpack_bf16x4(hi, b);
-  float ss = 0.0f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) ss = fmaf(b[k], b[k], fmaf(a[k], a[k], ss));
-  ss = group_sum<16>(ss);
-  const float r = __frsqrt_rn(ss * (1.0f / kHeadDim) + eps);
-  float wa[4], wb[4];
-  unpack_bf16x4(is_q ? w.q_lo : w.k_lo, wa);
-  unpack_bf16x4(is_q ? w.q_hi : w.k_hi, wb);
-  const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-  const float s[4] = {s4.x, s4.y, s4.z, s4.w};
-  float oa[4], ob[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float na = a[k] * r * wa[k];
-    const float nb = b[k] * r * wb[k];
-    oa[k] = fmaf(na, c[k], -nb * s[k]);
-    ob[k] = fmaf(nb, c[k], na * s[k]);
-  }
-  lo = make_uint2(pack_bf16x2(oa[0], oa[1]), pack_bf16x2(oa[2], oa[3]));
-  hi = make_uint2(pack_bf16x2(ob[0], ob[1]), pack_bf16x2(ob[2], ob[3]));
 }
 
 // One work item's rows as held by a lane: STEPS row fragments plus the
@@ -200,7 +153,7 @@ qk_tiles_kernel(const QkParams p) {
   const int item = blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (item >= p.items) return;  // whole warp leaves together
   QkWeights w;
-  load_weights(p, lane & 15, w);
+  qk128::load_weights(p.q_weight, p.k_weight, lane & 15, w);
   do_item<STEPS, CHECKED>(p, item, lane >> 4, lane & 15, w);
 }
 
@@ -212,7 +165,7 @@ qk_stream_kernel(const QkParams p) {
   const int nw = gridDim.x * WARPS;
   if (gw >= p.items) return;
   QkWeights w;
-  load_weights(p, lane & 15, w);
+  qk128::load_weights(p.q_weight, p.k_weight, lane & 15, w);
   for (int item = gw; item < p.items; item += nw) do_item<STEPS>(p, item, lane >> 4, lane & 15, w);
 }
 
@@ -267,16 +220,28 @@ cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+// Entries from here on are the TMA-staged shapes of kvq_qk_bulk.cu.
+constexpr int kQkFirstBulk = 7;
+
 const LaunchConfig kQkConfigs[] = {
     {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"}, {"tiles<8w,4step>"},
     {"stream<8w,4step>"}, {"general<frag4>"}, {"general<frag8>"},
+#define KVQ_BULK_NAME(W, S, R) {"bulk<" #W "w," #S "st," #R "r>"},
+    KVQ_QK_BULK_SHAPES(KVQ_BULK_NAME)
+#undef KVQ_BULK_NAME
 };
 const int kQkNumConfigs = sizeof(kQkConfigs) / sizeof(kQkConfigs[0]);
 
 cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream) {
   if (a.errors != nullptr) {  // bounds-checked: the two dispatch shapes
-    return config == 2 ? launch_tiles<4, 4, 1, true>(a, stream)
-                       : launch_tiles<4, 1, 1, true>(a, stream);
+    return config == 2 || config >= kQkFirstBulk ? launch_tiles<4, 4, 1, true>(a, stream)
+                                                 : launch_tiles<4, 1, 1, true>(a, stream);
+  }
+  if (config >= kQkFirstBulk && config < kQkFirstBulk + kQkBulkShapes) {
+    // Staged shapes need device memory for the bulk-copy engine; other
+    // buffers take the register-pipelined large-batch shape (same bits).
+    return qk_bulk_eligible(a, config - kQkFirstBulk) ? launch_qk_bulk(a, config - kQkFirstBulk, stream)
+                               : launch_tiles<4, 4, 1>(a, stream);
   }
   switch (config) {
     case 0: return launch_tiles<4, 1, 1>(a, stream);

@@ -197,6 +197,15 @@ def test_launch_config_table(L):
         kvq.set_config("dsv4", -1)
     assert kvq.dsv4_config_for(1, 1) in range(len(kvq.configs("dsv4")))
     assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))
+    qk = kvq.configs("qk")
+    # automatic QK shapes by Q+K head rows: < 1216 small-batch, < 131072
+    # register-pipelined, from there on TMA-staged
+    assert qk[kvq.qk_config_for(17, 16, 8)] == "tiles<4w,1step>"
+    assert qk[kvq.qk_config_for(30, 32, 8)] == "tiles<4w,1step>"   # 1200 rows
+    assert qk[kvq.qk_config_for(31, 32, 8)] == "tiles<4w,4step>"   # 1240 rows
+    assert qk[kvq.qk_config_for(3276, 32, 8)] == "tiles<4w,4step>"
+    assert qk[kvq.qk_config_for(3277, 32, 8)] == "bulk<24w,2st,12r>"
+    assert qk[kvq.qk_config_for(32768, 32, 8)] == "bulk<24w,2st,12r>"
 
 
 def test_gather_validation(L):

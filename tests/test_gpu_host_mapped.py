@@ -14,12 +14,19 @@ def _pinned(d, keys):
     return {k: (v.pin_memory() if k in keys else v) for k, v in d.items()}
 
 
-def test_qk_on_pinned_host_buffers(cuda_device):
+@pytest.mark.parametrize("config", [-1, 7], ids=["auto", "bulk"])
+def test_qk_on_pinned_host_buffers(cuda_device, config):
+    """Also with a TMA-staged shape forced: the bulk-copy engine is only given
+    device memory, so pinned buffers take the register-pipelined shape."""
     d = wl.make_qk(2048, 32, 8, 8, theta=1e6, max_pos=131072, seed=41, device="cpu")
     d = {k: (v.to(cuda_device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
     d["qkv"] = d["qkv"].cpu().pin_memory()
     d["positions"] = d["positions"].cpu().pin_memory()
-    qk_parity(d)
+    old = kvq.set_config("qk", config)
+    try:
+        qk_parity(d)
+    finally:
+        kvq.set_config("qk", old)
 
 
 def test_dsv4_on_pinned_host_buffers(cuda_device):

@@ -15,9 +15,12 @@ def test_decode_size_17_tokens(cuda_device):
     assert rep.exact_frac > 0.95
 
 
-def test_prefill_32768_tokens_every_token(cuda_device):
-    """The benchmarked workload, compared in full (1,310,720 head rows)."""
-    rep = qk_parity(wl.make_qk_workload(wl.QK_LARGE, device=cuda_device), slice_tokens=8192)
+@pytest.mark.parametrize("config", [-1, 7], ids=["auto", "bulk"])
+def test_prefill_32768_tokens_every_token(cuda_device, config):
+    """The benchmarked workload, compared in full (1,310,720 head rows), under
+    the automatic dispatch and under a TMA-staged shape."""
+    with with_config("qk", config):
+        rep = qk_parity(wl.make_qk_workload(wl.QK_LARGE, device=cuda_device), slice_tokens=8192)
     assert rep.n == 32768 * 40 * 128
     assert rep.exact_frac > 0.95
 
@@ -84,7 +87,7 @@ def test_runs_on_a_side_stream(cuda_device):
     assert torch.equal(d["qkv"], ref["qkv"])
 
 
-QK_CONFIGS = list(range(7))
+QK_CONFIGS = list(range(10))
 
 
 @pytest.mark.parametrize("config", QK_CONFIGS)
@@ -110,7 +113,7 @@ def test_general_layouts(cuda_device, layout, shape, config):
     """head_dim 64/128/256, NeoX or GPT-J pairs, full or partial rotation,
     through the general kernel (automatic choice, then 4- and 8-dim fragments
     forced), against the oracle."""
-    assert kvq.configs("qk")[5:] == ["general<frag4>", "general<frag8>"]
+    assert kvq.configs("qk")[5:7] == ["general<frag4>", "general<frag8>"]
     D, rot, neox = layout
     T, Hq, Hk, Hv = shape
     d = wl.make_qk(T, Hq, Hk, Hv, D=D, theta=1e4, max_pos=8192, seed=D + rot + T,
@@ -125,3 +128,48 @@ def test_general_layout_at_scale(cuda_device):
     d = wl.make_qk(32768, 16, 4, 4, D=256, theta=1e6, max_pos=131072, seed=77,
                    device=cuda_device, rotary_dim=64, is_neox=False)
     qk_parity(d, slice_tokens=8192)
+
+
+BULK = list(range(7, 10))   # the TMA-staged shapes
+TUNED_SHAPES = [0, 1, 2, 3, 4] + BULK   # every launch shape of the D=128 NeoX kernels
+
+
+def _run_config(d, config):
+    out = d["qkv"].clone()
+    with with_config("qk", config):
+        kvq.fused_qk_norm_rope(out, d["Hq"], d["Hk"], d["Hv"], 128, d["eps"], d["q_weight"],
+                               d["k_weight"], d["cos_sin"], True, d["positions"])
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("shape", [(4096, 32, 8, 8), (777, 5, 3, 2), (1, 16, 8, 8),
+                                   (300, 64, 8, 8), (50, 100, 28, 3)])
+def test_launch_shapes_bit_identical(cuda_device, shape):
+    """The register-pipelined and the TMA-staged shapes share the row
+    arithmetic: every one gives the same bits."""
+    assert [n.startswith("bulk") for n in kvq.configs("qk")] == [False] * 7 + [True] * 3
+    T, Hq, Hk, Hv = shape
+    d = wl.make_qk(T, Hq, Hk, Hv, theta=1e6, max_pos=131072, seed=T + Hq, device=cuda_device)
+    ref = _run_config(d, 2)
+    assert not torch.equal(ref, d["qkv"])
+    for config in TUNED_SHAPES:
+        assert torch.equal(_run_config(d, config), ref), kvq.configs("qk")[config]
+
+
+@pytest.mark.parametrize("config", BULK)
+def test_staged_shape_finishing_from_global_memory(cuda_device, config):
+    """With a stage-wait limit of 0 every warp of a staged launch gives up on
+    its first wait: it lets its copies land, then finishes every item with
+    direct loads.  The results are the same bits, and match the oracle."""
+    d = wl.make_qk(2000, 32, 8, 8, theta=1e6, max_pos=131072, seed=61, device=cuda_device)
+    ref = _run_config(d, 2)
+    old = kvq.set_qk_stage_wait_limit(0)
+    try:
+        assert old > 0
+        assert torch.equal(_run_config(d, config), ref)
+        with with_config("qk", config):
+            qk_parity(d)
+    finally:
+        kvq.set_qk_stage_wait_limit(old)
+    assert kvq.set_qk_stage_wait_limit(old) == old
