@@ -607,9 +607,10 @@ def sweep(kvq, device):
     emit({"sweep": "d2d_copy_qk_T32768_bytes", "bytes": nb, "us_median": round(med * 1e3, 2),
           "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1)})
     del src, dst
-    # the general QK kernel (head_dim 64/256, GPT-J pairs, partial rotation):
-    # the automatic choice and both fragment widths forced
-    general = [(i, n) for i, n in enumerate(kvq.configs("qk")) if n.startswith("general")]
+    # the general QK layouts (head_dim 64/256, GPT-J pairs, partial rotation):
+    # the automatic choice, both one-shot fragment widths and the staged shapes
+    general = [(i, n) for i, n in enumerate(kvq.configs("qk"))
+               if n.startswith("general") or n.startswith("bulk")]
     for (T, hq, hk, hv, D, rot, neox) in ((32768, 32, 8, 8, 64, 64, True),
                                           (32768, 32, 8, 8, 64, 32, False),
                                           (32768, 32, 8, 8, 128, 64, True),

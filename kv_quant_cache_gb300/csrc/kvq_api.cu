@@ -22,7 +22,7 @@ constexpr int kDsv4SmallConfig = 0;  // tiles<4w,1row>
 constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg>
 constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
 constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
-constexpr int kQkStagedConfig = 8;   // bulk<24w,2st,12r>
+constexpr int kQkStagedConfig = 7;   // bulk<16w,2st,6KB>
 // Entries of kQkConfigs that name the general kernel (any layout) with 4- or
 // 8-dim fragments; forcing one routes every layout through that kernel.
 constexpr int kQkGeneralFrag4Config = 5;
@@ -30,11 +30,14 @@ constexpr int kQkGeneralFrag8Config = 6;
 // Fragment width the general kernel takes for layouts outside the tuned one.
 constexpr int kQkGeneralFrag = 4;
 // Q+K head rows below which the QK operator takes its small-batch shape, and
-// from which it takes the TMA-staged shape (measured on GB300 by the
-// benchmark's QK crossover sweep: the staged shape ties the register-pipelined
-// one near 80K rows and wins from 160K rows on, by 6-11 % at 2.6M-5.2M rows).
+// from which it takes the TMA-staged shape (every layout).  Measured on GB300
+// by the benchmark's QK sweeps: at head_dim 128 the staged and the
+// register-pipelined shapes are within a few percent of each other between
+// 160K and 655K rows, the staged shape leads from 1.3M rows on (93 % vs 91 %
+// of the copy peak) and by 11 % at 5.2M rows; for the other layouts it leads
+// the one-shot general kernel by 2-10 % at 650K-1.3M rows.
 constexpr int64_t kQkSmallRows = 152 * 8;
-constexpr int64_t kQkStagedRows = 131072;
+constexpr int64_t kQkStagedRows = (int64_t)1 << 20;
 
 std::atomic<int64_t> g_threshold{-1};
 std::atomic<int> g_dsv4_config{-1};
@@ -156,9 +159,13 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   if (config == kQkGeneralFrag4Config || config == kQkGeneralFrag8Config)
     return finish_launch(
         kvq::launch_qk_general(a, small, config == kQkGeneralFrag8Config ? 8 : 4, st));
+  // TMA-staged shapes serve every layout, unchecked calls on device memory.
+  const int shape = config - kvq::kQkFirstBulk;
+  if (errors == nullptr && shape >= 0 && kvq::qk_bulk_eligible(a, shape))
+    return finish_launch(kvq::launch_qk_bulk(a, shape, st));
   if (head_dim == 128 && is_neox == 1 && rotary_dim == 128)
     return finish_launch(kvq::launch_qk_norm_rope(a, config, st));
-  return finish_launch(kvq::launch_qk_general(a, small, kQkGeneralFrag, st));
+  return finish_launch(kvq::launch_qk_general(a, small && shape < 0, kQkGeneralFrag, st));
 }
 
 kvq_status dsv4_impl(const void* q, void* q_out, const void* kv, int64_t num_tokens,

@@ -1,28 +1,30 @@
-// kvq_qk_bulk.cu -- the head_dim-128 full-NeoX QK operator with its inputs
-// staged in shared memory by the bulk-copy (TMA) engine.
+// kvq_qk_bulk.cu -- the packed-QKV operator (every supported layout: head_dim
+// 64 / 128 / 256, NeoX or GPT-J pairs, full or partial rotation) with its
+// inputs staged in shared memory by the bulk-copy (TMA) engine.
 //
-// Operator and row arithmetic: those of kvq_qk_norm_rope.cu (InfiniOps PR
-// #1019, "Add the NineToothed NVIDIA implementation of FusedQkNormRope",
-// section "Summary"), shared through kvq_qk_row.cuh, so the results are
-// bit-identical to every other launch shape of the operator.
+// Operator and row arithmetic: those of InfiniOps PR #1019 ("Add the
+// NineToothed NVIDIA implementation of FusedQkNormRope", section "Summary"),
+// shared with the one-shot kernels through kvq_qk_general_row.cuh, so the
+// results are the same bits.
 //
 // Mapping on sm_103a.  A persistent grid (resident CTAs x SMs).  Each warp
 // owns a ring of NS shared-memory stages with one mbarrier per stage and takes
 // the work items gw, gw + W, gw + 2W, ... (W = warps in the grid), so at any
 // moment the grid works on one contiguous window of qkv.  A work item is
 // (token, chunk of at most RMAX consecutive Q/K head rows, the chunks of a
-// token balanced in length).  Its rows are one contiguous span of qkv and
-// arrive with one cp.async.bulk; the token's cos/sin row (512 bytes) arrives
-// with a second; both complete on the stage's mbarrier, and both carry an L2
-// evict-first policy (each byte is read once).  Lane 0 keeps NS items in
-// flight: when the warp has consumed a stage it issues the item NS ahead
-// into it.  The positions of the warp's next 32 items are fetched one per
-// lane, a window ahead, so no copy waits on a position load.  All 32 lanes
-// wait on the stage's barrier; then the half-warps take alternate rows, U row
-// pairs at a time (independent rows, so their shuffles overlap), reading
-// their 8-byte fragments and their cosines and sines from shared memory, and
-// write the results straight to global memory with evict-first stores.  V
-// columns are never addressed.
+// token balanced in length); a stage holds STAGE_BYTES of rows, so RMAX =
+// STAGE_BYTES / (2 D).  The item's rows are one contiguous span of qkv and
+// arrive with one cp.async.bulk; the token's cos/sin row (4 rot bytes)
+// arrives with a second; both complete on the stage's mbarrier, and both
+// carry an L2 evict-first policy (each byte is read once).  Lane 0 keeps NS
+// items in flight: when the warp has consumed a stage it issues the item NS
+// ahead into it.  The positions of the warp's next 32 items are fetched one
+// per lane, a window ahead, so no copy waits on a position load.  All 32
+// lanes wait on the stage's barrier; then each group of D/8 lanes takes a
+// row, four rows per group at a time (independent rows, so their shuffles
+// overlap), reading its fragments and its cosines and sines from shared
+// memory, and the results go straight to global memory with evict-first
+// stores.  V columns are never addressed.
 //
 // Every wait is bounded.  A warp that has polled a stage barrier `wait_limit`
 // times, or for 20 ms, stops staging: it first waits (bounded again) for the
@@ -34,18 +36,15 @@
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 #include "kvq_qk_bulk.h"
-#include "kvq_qk_row.cuh"
+#include "kvq_qk_general_row.cuh"
 
 namespace kvq {
 namespace {
 
-using qk128::kHeadDim;
-using qk128::row_math;
-using qk128::Weights;
-
-constexpr int kRowBytes = kHeadDim * 2;  // one bf16 head row
-constexpr int kCsBytes = kHeadDim * 4;   // one fp32 cos/sin row
-constexpr int kUnroll = 4;               // row pairs computed together
+using qkgen::Lane;
+using Frag4 = qkgen::Frag<4>;
+constexpr int kF = 4;                    // dims per fragment
+constexpr int kUnroll = 4;               // row steps computed together
 constexpr uint32_t kDefaultWaitLimit = 1u << 22;
 constexpr uint64_t kWaitNs = 20000000;   // 20 ms: a stage wait then gives up
 constexpr uint32_t kDrainPolls = 1u << 22;
@@ -59,9 +58,10 @@ struct BulkParams {
   const __nv_bfloat16* k_weight;
   const float* cos_sin;
   const int64_t* positions;
-  int64_t row_elems;  // (Hq + Hk + Hv) * 128
+  int64_t row_elems;  // (Hq + Hk + Hv) * D
   int num_q;          // Hq
   int num_rows;       // Hq + Hk
+  int rot;            // rotary_dim
   int chunks;         // work items per token
   int chunk_rows;     // rows of every chunk but possibly the token's last
   int items;          // num_tokens * chunks
@@ -69,7 +69,7 @@ struct BulkParams {
   uint32_t wait_limit;
 };
 
-// ---- inline PTX: mbarrier, bulk copy, cache policy, proxy fences ----------
+// ---- inline PTX: mbarrier, bulk copy, cache policy, proxy fence, timer -----
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -110,15 +110,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Polls the completion of the barrier phase with parity `parity` at most
-// `limit` times and for at most `ns` nanoseconds; the result is the same on
-// every lane of the warp.
+// `limit` times and for about `ns` nanoseconds at most (the clock is read
+// every 64 polls); the result is the same on every lane of the warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t limit,
                                                uint64_t ns) {
-  bool done = false;
-  const uint64_t t0 = limit ? global_ns() : 0;
-  for (uint32_t i = 0; i < limit && !done; ++i) {
-    done = mbar_test(bar, parity);
-    if (!done && global_ns() - t0 > ns) break;
+  bool done = limit > 0 && mbar_test(bar, parity);
+  if (!done && limit > 1) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < limit; ++i) {
+      if ((done = mbar_test(bar, parity))) break;
+      if ((i & 63u) == 0 && global_ns() - t0 > ns) break;
+    }
   }
   return __all_sync(kFullMask, done);
 }
@@ -146,7 +148,7 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---- work items --------------------------------------------------------------
+// ---- work items -------------------------------------------------------------
 
 struct Item {
   int t, r0, nr;  // token, first row, rows
@@ -160,67 +162,70 @@ __device__ __forceinline__ Item item_at(const BulkParams& p, int item) {
   return it;
 }
 
-// The rows of one item: fragments read by `fetch(j, lo, hi)` (row j of the
-// item), normalised and rotated, and handed to `put(j, lo, hi)`.  Half-warp
-// `half` takes rows half, half + 2, ...; the trip count is warp-uniform.
-template <typename Fetch, typename Put>
-__device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, int half,
-                                          const Weights& w, const float4& c4, const float4& s4,
-                                          Fetch fetch, Put put) {
-  for (int j0 = 0; j0 < it.nr; j0 += 2 * kUnroll) {
-    uint2 lo[kUnroll], hi[kUnroll];
+// Row j of an item in global memory.
+template <int D>
+__device__ __forceinline__ __nv_bfloat16* global_row(const BulkParams& p, const Item& it, int j) {
+  return p.qkv + (size_t)it.t * (size_t)p.row_elems + (size_t)(it.r0 + j) * D;
+}
+
+// The lane's packed Q and K weights at its two fragments.
+struct Weights {
+  uint2 qa, qb, ka, kb;
+};
+
+// The rows of one item: lane group g (of 32 / (D/8)) takes rows g, g + RPW,
+// ...; `rows` points at the item's first row (shared or global memory),
+// `angles` at the token's cos/sin row.  The trip count is warp-uniform.
+template <int D, bool NEOX, bool SMEM>
+__device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, int g, int l,
+                                          const Lane<D, kF, NEOX>& ln, const Weights& w,
+                                          const __nv_bfloat16* rows, const float* angles) {
+  constexpr int RPW = 32 / (D / (2 * kF));  // rows per warp step
+  float cs[kF], sn[kF];
+  qkgen::lane_angles<D, kF, NEOX, !SMEM>(angles, l, p.rot, ln, cs, sn);
+  for (int j0 = 0; j0 < it.nr; j0 += RPW * kUnroll) {
+    uint2 xa[kUnroll], xb[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int j = j0 + 2 * u + half;
-      lo[u] = hi[u] = make_uint2(0u, 0u);
-      if (j < it.nr) fetch(j, lo[u], hi[u]);
+      const int j = j0 + RPW * u + g;
+      xa[u] = xb[u] = Frag4::zero();
+      if (j < it.nr) {
+        const __nv_bfloat16* row = rows + (size_t)j * D;
+        if (SMEM) {
+          xa[u] = *reinterpret_cast<const uint2*>(row + ln.oa);
+          xb[u] = *reinterpret_cast<const uint2*>(row + ln.ob);
+        } else {
+          xa[u] = __ldcs(reinterpret_cast<const uint2*>(row + ln.oa));
+          xb[u] = __ldcs(reinterpret_cast<const uint2*>(row + ln.ob));
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (j0 + 2 * u >= it.nr) break;  // warp-uniform: no row left for either half
-      const int j = j0 + 2 * u + half;
-      row_math(lo[u], hi[u], it.r0 + j < p.num_q, w, c4, s4, p.eps);
-      if (j < it.nr) put(j, lo[u], hi[u]);
+      if (j0 + RPW * u >= it.nr) break;  // warp-uniform: no row left for any group
+      const int j = j0 + RPW * u + g;
+      const bool is_q = it.r0 + j < p.num_q;
+      qkgen::row_math<D, kF, NEOX>(xa[u], xb[u], is_q ? w.qa : w.ka, is_q ? w.qb : w.kb, cs, sn,
+                                   ln, p.eps);
+      if (j < it.nr) {
+        __nv_bfloat16* row = global_row<D>(p, it, j);
+        __stcs(reinterpret_cast<uint2*>(row + ln.oa), xa[u]);
+        __stcs(reinterpret_cast<uint2*>(row + ln.ob), xb[u]);
+      }
     }
   }
 }
 
-// Row j of an item in global memory.
-__device__ __forceinline__ uint2* global_row(const BulkParams& p, const Item& it, int j) {
-  return reinterpret_cast<uint2*>(p.qkv + (size_t)it.t * (size_t)p.row_elems +
-                                  (size_t)(it.r0 + j) * kHeadDim);
-}
-
-// An item straight from global memory (the path after a wait ran out).
-__device__ __forceinline__ void direct_item(const BulkParams& p, int item, int half, int l16,
-                                            const Weights& w) {
-  const Item it = item_at(p, item);
-  const int64_t pos = __ldg(p.positions + it.t);
-  const float4* cs = reinterpret_cast<const float4*>(p.cos_sin + pos * kHeadDim);
-  const float4 c4 = __ldg(cs + l16);
-  const float4 s4 = __ldg(cs + 16 + l16);
-  item_rows(
-      p, it, half, w, c4, s4,
-      [&](int j, uint2& lo, uint2& hi) {
-        const uint2* row = global_row(p, it, j);
-        lo = __ldcs(row + l16);
-        hi = __ldcs(row + 16 + l16);
-      },
-      [&](int j, const uint2& lo, const uint2& hi) {
-        uint2* row = global_row(p, it, j);
-        __stcs(row + l16, lo);
-        __stcs(row + 16 + l16, hi);
-      });
-}
-
-template <int WARPS, int NS, int RMAX>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 qk_bulk_kernel(const BulkParams p) {
-  constexpr int kCsAt = RMAX * kRowBytes;       // cos/sin row inside a stage
-  constexpr int kStage = kCsAt + kCsBytes;      // a multiple of 128 bytes
+  constexpr int kCsAt = STAGE_BYTES;           // cos/sin row inside a stage
+  constexpr int kStage = STAGE_BYTES + 4 * D;  // room for a full-width cos/sin row
+  constexpr int LPR = D / (2 * kF);            // lanes per row
+  static_assert(kStage % 128 == 0, "stage alignment");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, l16 = lane & 15;
+  const int g = lane / LPR, l = lane % LPR;
   const int gw = blockIdx.x * WARPS + warp;
   const int nw = gridDim.x * WARPS;
   if (gw >= p.items) return;                    // whole warp leaves together
@@ -235,9 +240,14 @@ qk_bulk_kernel(const BulkParams p) {
     mbar_init_fence();
   }
   __syncwarp();
+  const Lane<D, kF, NEOX> ln(l, p.rot);
   Weights w;
-  qk128::load_weights(p.q_weight, p.k_weight, l16, w);
+  w.qa = __ldg(reinterpret_cast<const uint2*>(p.q_weight + ln.oa));
+  w.qb = __ldg(reinterpret_cast<const uint2*>(p.q_weight + ln.ob));
+  w.ka = __ldg(reinterpret_cast<const uint2*>(p.k_weight + ln.oa));
+  w.kb = __ldg(reinterpret_cast<const uint2*>(p.k_weight + ln.ob));
   const uint64_t pol = evict_first_policy();
+  const uint32_t cs_bytes = 4u * (uint32_t)p.rot;
 
   // Positions of issue window [wb, wb + 32) (one per lane) and of the next.
   auto position = [&](int k) -> int64_t {
@@ -246,8 +256,8 @@ qk_bulk_kernel(const BulkParams p) {
   int wb = 0;
   int64_t pos_cur = position(lane), pos_next = position(32 + lane);
 
-  // Copies of item k into stage k % NS; every lane calls, lane 0 issues.
-  // Issued in order k = 0, 1, 2, ...
+  // Copies of item k into stage k % NS, issued in order k = 0, 1, 2, ...;
+  // every lane calls, lane 0 issues.
   auto issue = [&](int k) {
     if (k >= n) return;  // warp-uniform
     if (k - wb == 32) {
@@ -260,11 +270,11 @@ qk_bulk_kernel(const BulkParams p) {
       const Item it = item_at(p, gw + k * nw);
       const uint32_t stage = ring_s + (uint32_t)(k % NS) * kStage;
       const uint32_t bar = bar0 + 8u * (k % NS);
-      const uint32_t bytes = (uint32_t)it.nr * kRowBytes;
+      const uint32_t bytes = (uint32_t)it.nr * (2u * D);
       fence_proxy_async();
-      mbar_arrive_expect_tx(bar, bytes + kCsBytes);
-      bulk_load(stage, global_row(p, it, 0), bytes, bar, pol);
-      bulk_load(stage + kCsAt, p.cos_sin + pos * kHeadDim, kCsBytes, bar, pol);
+      mbar_arrive_expect_tx(bar, bytes + cs_bytes);
+      bulk_load(stage, global_row<D>(p, it, 0), bytes, bar, pol);
+      bulk_load(stage + kCsAt, p.cos_sin + pos * p.rot, cs_bytes, bar, pol);
     }
   };
 
@@ -274,44 +284,37 @@ qk_bulk_kernel(const BulkParams p) {
   for (; k < n; ++k) {
     if (!mbar_wait_warp(bar0 + 8u * (k % NS), (uint32_t)(k / NS) & 1u, p.wait_limit, kWaitNs))
       break;
-    const Item it = item_at(p, gw + k * nw);
     const uint8_t* stage = ring + (size_t)(k % NS) * kStage;
-    const float4 c4 = *reinterpret_cast<const float4*>(stage + kCsAt + 16 * l16);
-    const float4 s4 = *reinterpret_cast<const float4*>(stage + kCsAt + 256 + 16 * l16);
-    item_rows(
-        p, it, half, w, c4, s4,
-        [&](int j, uint2& lo, uint2& hi) {
-          const uint2* row = reinterpret_cast<const uint2*>(stage + j * kRowBytes);
-          lo = row[l16];
-          hi = row[16 + l16];
-        },
-        [&](int j, const uint2& lo, const uint2& hi) {
-          uint2* row = global_row(p, it, j);
-          __stcs(row + l16, lo);
-          __stcs(row + 16 + l16, hi);
-        });
+    item_rows<D, NEOX, true>(p, item_at(p, gw + k * nw), g, l, ln, w,
+                             reinterpret_cast<const __nv_bfloat16*>(stage),
+                             reinterpret_cast<const float*>(stage + kCsAt));
     __syncwarp();
     issue(k + NS);
   }
   if (k < n) {
     // A wait ran out: let the copies still in flight (items k .. k+NS-1)
-    // land before this warp's shared memory can be reused, then finish.
+    // land before this warp's shared memory can be reused, then finish from
+    // global memory.
     for (int q = k; q < n && q < k + NS; ++q)
       mbar_wait_warp(bar0 + 8u * (q % NS), (uint32_t)(q / NS) & 1u, kDrainPolls, kDrainNs);
-    for (; k < n; ++k) direct_item(p, gw + k * nw, half, l16, w);
+    for (; k < n; ++k) {
+      const Item it = item_at(p, gw + k * nw);
+      item_rows<D, NEOX, false>(p, it, g, l, ln, w, global_row<D>(p, it, 0),
+                                p.cos_sin + __ldg(p.positions + it.t) * p.rot);
+    }
   }
 }
 
-// ---- launch ---------------------------------------------------------------------
+// ---- launch -------------------------------------------------------------------
 
-template <int WARPS, int NS, int RMAX>
+template <int D, int WARPS, int NS, int STAGE_BYTES>
 constexpr size_t smem_bytes() {
-  return (size_t)WARPS * NS * (RMAX * kRowBytes + kCsBytes) + (size_t)WARPS * NS * 8;
+  return (size_t)WARPS * NS * (STAGE_BYTES + 4 * D) + (size_t)WARPS * NS * 8;
 }
 
 // Opts the kernel in to its shared memory and counts its resident CTAs per
 // SM, once per device.
-template <int WARPS, int NS, int RMAX>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
 cudaError_t prepare(int* per_sm) {
   static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
@@ -325,8 +328,8 @@ cudaError_t prepare(int* per_sm) {
       return cudaSuccess;
     }
   }
-  auto kernel = qk_bulk_kernel<WARPS, NS, RMAX>;
-  constexpr size_t bytes = smem_bytes<WARPS, NS, RMAX>();
+  auto kernel = qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>;
+  constexpr size_t bytes = smem_bytes<D, WARPS, NS, STAGE_BYTES>();
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   int n = 0;
@@ -344,12 +347,11 @@ void chunking(const QkArgs& a, int rmax, int* chunks, int* chunk_rows) {
   *chunk_rows = (rows + *chunks - 1) / *chunks;
 }
 
-template <int WARPS, int NS, int RMAX>
-cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
-  static_assert((RMAX * kRowBytes + kCsBytes) % 128 == 0, "stage alignment");
-  static_assert(smem_bytes<WARPS, NS, RMAX>() <= 227 * 1024, "shared memory per CTA");
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
+cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
+  static_assert(smem_bytes<D, WARPS, NS, STAGE_BYTES>() <= 227 * 1024, "shared memory per CTA");
   int per_sm = 0;
-  cudaError_t e = prepare<WARPS, NS, RMAX>(&per_sm);
+  cudaError_t e = prepare<D, NEOX, WARPS, NS, STAGE_BYTES>(&per_sm);
   if (e != cudaSuccess) return e;
   BulkParams p;
   p.qkv = static_cast<__nv_bfloat16*>(a.qkv);
@@ -359,8 +361,9 @@ cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
   p.positions = a.positions;
   p.num_q = a.num_heads_q;
   p.num_rows = a.num_heads_q + a.num_heads_k;
-  p.row_elems = (int64_t)(p.num_rows + a.num_heads_v) * kHeadDim;
-  chunking(a, RMAX, &p.chunks, &p.chunk_rows);
+  p.row_elems = (int64_t)(p.num_rows + a.num_heads_v) * D;
+  p.rot = a.rotary_dim;
+  chunking(a, STAGE_BYTES / (2 * D), &p.chunks, &p.chunk_rows);
   p.items = a.num_tokens * p.chunks;
   p.eps = a.eps;
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
@@ -368,9 +371,26 @@ cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
   const int64_t need = (p.items + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  qk_bulk_kernel<WARPS, NS, RMAX>
-      <<<(unsigned)grid, WARPS * 32, smem_bytes<WARPS, NS, RMAX>(), stream>>>(p);
+  qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>
+      <<<(unsigned)grid, WARPS * 32, smem_bytes<D, WARPS, NS, STAGE_BYTES>(), stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int WARPS, int NS, int STAGE_BYTES>
+cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
+  const bool neox = a.is_neox != 0;
+  switch (a.head_dim) {
+    case 64:
+      return neox ? launch_layout<64, true, WARPS, NS, STAGE_BYTES>(a, stream)
+                  : launch_layout<64, false, WARPS, NS, STAGE_BYTES>(a, stream);
+    case 128:
+      return neox ? launch_layout<128, true, WARPS, NS, STAGE_BYTES>(a, stream)
+                  : launch_layout<128, false, WARPS, NS, STAGE_BYTES>(a, stream);
+    case 256:
+      return neox ? launch_layout<256, true, WARPS, NS, STAGE_BYTES>(a, stream)
+                  : launch_layout<256, false, WARPS, NS, STAGE_BYTES>(a, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 bool device_memory(const void* ptr) {
@@ -385,15 +405,15 @@ bool device_memory(const void* ptr) {
 }  // namespace
 
 bool qk_bulk_eligible(const QkArgs& a, int shape) {
-  static constexpr int kRows[] = {
-#define KVQ_ROWS(W, S, R) R,
-      KVQ_QK_BULK_SHAPES(KVQ_ROWS)
-#undef KVQ_ROWS
+  static constexpr int kStageBytes[] = {
+#define KVQ_STAGE(W, S, KB) KB * 1024,
+      KVQ_QK_BULK_SHAPES(KVQ_STAGE)
+#undef KVQ_STAGE
   };
   if (shape < 0 || shape >= kQkBulkShapes) return false;
-  if (a.head_dim != kHeadDim || a.is_neox != 1 || a.rotary_dim != kHeadDim) return false;
+  if (a.head_dim != 64 && a.head_dim != 128 && a.head_dim != 256) return false;
   int chunks = 0, chunk_rows = 0;
-  chunking(a, kRows[shape], &chunks, &chunk_rows);
+  chunking(a, kStageBytes[shape] / (2 * a.head_dim), &chunks, &chunk_rows);
   if ((int64_t)(chunks - 1) * chunk_rows >= a.num_heads_q + a.num_heads_k) return false;
   return device_memory(a.qkv) && device_memory(a.cos_sin);
 }
@@ -401,7 +421,7 @@ bool qk_bulk_eligible(const QkArgs& a, int shape) {
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream) {
   using Launch = cudaError_t (*)(const QkArgs&, cudaStream_t);
   static constexpr Launch kLaunch[] = {
-#define KVQ_LAUNCH(W, S, R) &launch_shape<W, S, R>,
+#define KVQ_LAUNCH(W, S, KB) &launch_shape<W, S, KB * 1024>,
       KVQ_QK_BULK_SHAPES(KVQ_LAUNCH)
 #undef KVQ_LAUNCH
   };

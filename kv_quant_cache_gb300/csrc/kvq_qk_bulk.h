@@ -9,20 +9,24 @@
 
 namespace kvq {
 
-// Staged launch shapes X(warps per CTA, stages per warp, rows per stage), in
-// the order of their QK configuration entries (named bulk<Ww,Sst,Rr>).
-#define KVQ_QK_BULK_SHAPES(X) X(16, 2, 24) X(24, 2, 12) X(24, 3, 8)
-#define KVQ_QK_BULK_COUNT(W, S, R) +1
+// Staged launch shapes X(warps per CTA, stages per warp, KB of head rows per
+// stage), in the order of their QK configuration entries (named
+// bulk<Ww,Sst,KKB>).  A stage holds KB * 1024 / (2 head_dim) rows plus one
+// cos/sin row.
+#define KVQ_QK_BULK_SHAPES(X) X(16, 2, 6) X(24, 2, 3) X(24, 3, 2)
+#define KVQ_QK_BULK_COUNT(W, S, KB) +1
 constexpr int kQkBulkShapes = 0 KVQ_QK_BULK_SHAPES(KVQ_QK_BULK_COUNT);
+// Index of the first staged shape in the QK configuration table.
+constexpr int kQkFirstBulk = 7;
 
-// True when staged shape `shape` may serve this call: the head_dim-128
-// full-NeoX layout, qkv and the cos/sin table in device memory (the
-// bulk-copy engine is not pointed at mapped host memory), and the token's
-// rows split into non-empty chunks.
+// True when staged shape `shape` may serve this call: a supported head_dim,
+// qkv and the cos/sin table in device memory (the bulk-copy engine is not
+// pointed at mapped host memory), and the token's rows split into non-empty
+// chunks.
 bool qk_bulk_eligible(const QkArgs& a, int shape);
 
-// Launch staged shape `shape` (0 .. kQkBulkShapes-1) of the head_dim-128
-// full-NeoX operator.
+// Launch staged shape `shape` (0 .. kQkBulkShapes-1) for any supported
+// layout (head_dim 64 / 128 / 256, NeoX or GPT-J, full or partial rotation).
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream);
 
 // Polls of a stage barrier after which a warp stops staging and finishes its

@@ -220,13 +220,10 @@ cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-// Entries from here on are the TMA-staged shapes of kvq_qk_bulk.cu.
-constexpr int kQkFirstBulk = 7;
-
 const LaunchConfig kQkConfigs[] = {
     {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"}, {"tiles<8w,4step>"},
     {"stream<8w,4step>"}, {"general<frag4>"}, {"general<frag8>"},
-#define KVQ_BULK_NAME(W, S, R) {"bulk<" #W "w," #S "st," #R "r>"},
+#define KVQ_BULK_NAME(W, S, KB) {"bulk<" #W "w," #S "st," #KB "KB>"},
     KVQ_QK_BULK_SHAPES(KVQ_BULK_NAME)
 #undef KVQ_BULK_NAME
 };
@@ -237,12 +234,9 @@ cudaError_t launch_qk_norm_rope(const QkArgs& a, int config, cudaStream_t stream
     return config == 2 || config >= kQkFirstBulk ? launch_tiles<4, 4, 1, true>(a, stream)
                                                  : launch_tiles<4, 1, 1, true>(a, stream);
   }
-  if (config >= kQkFirstBulk && config < kQkFirstBulk + kQkBulkShapes) {
-    // Staged shapes need device memory for the bulk-copy engine; other
-    // buffers take the register-pipelined large-batch shape (same bits).
-    return qk_bulk_eligible(a, config - kQkFirstBulk) ? launch_qk_bulk(a, config - kQkFirstBulk, stream)
-                               : launch_tiles<4, 4, 1>(a, stream);
-  }
+  // A staged shape that the call is not eligible for: the register-pipelined
+  // large-batch shape (same bits).
+  if (config >= kQkFirstBulk) return launch_tiles<4, 4, 1>(a, stream);
   switch (config) {
     case 0: return launch_tiles<4, 1, 1>(a, stream);
     case 1: return launch_tiles<8, 2, 1>(a, stream);

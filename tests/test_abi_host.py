@@ -198,14 +198,14 @@ def test_launch_config_table(L):
     assert kvq.dsv4_config_for(1, 1) in range(len(kvq.configs("dsv4")))
     assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))
     qk = kvq.configs("qk")
-    # automatic QK shapes by Q+K head rows: < 1216 small-batch, < 131072
+    # automatic QK shapes by Q+K head rows: < 1216 small-batch, < 2^20
     # register-pipelined, from there on TMA-staged
     assert qk[kvq.qk_config_for(17, 16, 8)] == "tiles<4w,1step>"
     assert qk[kvq.qk_config_for(30, 32, 8)] == "tiles<4w,1step>"   # 1200 rows
     assert qk[kvq.qk_config_for(31, 32, 8)] == "tiles<4w,4step>"   # 1240 rows
-    assert qk[kvq.qk_config_for(3276, 32, 8)] == "tiles<4w,4step>"
-    assert qk[kvq.qk_config_for(3277, 32, 8)] == "bulk<24w,2st,12r>"
-    assert qk[kvq.qk_config_for(32768, 32, 8)] == "bulk<24w,2st,12r>"
+    assert qk[kvq.qk_config_for(26214, 32, 8)] == "tiles<4w,4step>"   # 1048560 rows
+    assert qk[kvq.qk_config_for(26215, 32, 8)] == "bulk<16w,2st,6KB>"
+    assert qk[kvq.qk_config_for(32768, 32, 8)] == "bulk<16w,2st,6KB>"
 
 
 def test_gather_validation(L):

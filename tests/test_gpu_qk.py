@@ -106,13 +106,14 @@ LAYOUTS = [(D, rot, neox) for D in (64, 128, 256) for neox in (True, False)
            for rot in sorted({16, D // 2, D}) if rot % 16 == 0 and not (D == 128 and rot == 128 and neox)]
 
 
-@pytest.mark.parametrize("config", [-1, 5, 6], ids=["auto", "frag4", "frag8"])
+@pytest.mark.parametrize("config", [-1, 5, 6, 7, 8, 9],
+                         ids=["auto", "frag4", "frag8", "bulk6KB", "bulk3KB", "bulk2KB"])
 @pytest.mark.parametrize("layout", LAYOUTS, ids=lambda l: f"D{l[0]}_rot{l[1]}_{'neox' if l[2] else 'gptj'}")
 @pytest.mark.parametrize("shape", [(1, 4, 2, 1), (17, 3, 1, 2), (777, 8, 2, 2), (300, 0, 5, 0)])
 def test_general_layouts(cuda_device, layout, shape, config):
     """head_dim 64/128/256, NeoX or GPT-J pairs, full or partial rotation,
-    through the general kernel (automatic choice, then 4- and 8-dim fragments
-    forced), against the oracle."""
+    through the one-shot general kernel (automatic choice, 4- and 8-dim
+    fragments forced) and the TMA-staged shapes, against the oracle."""
     assert kvq.configs("qk")[5:7] == ["general<frag4>", "general<frag8>"]
     D, rot, neox = layout
     T, Hq, Hk, Hv = shape
@@ -131,7 +132,7 @@ def test_general_layout_at_scale(cuda_device):
 
 
 BULK = list(range(7, 10))   # the TMA-staged shapes
-TUNED_SHAPES = [0, 1, 2, 3, 4] + BULK   # every launch shape of the D=128 NeoX kernels
+TUNED_SHAPES = [0, 1, 2, 3, 4, 5] + BULK   # every 4-dim-fragment shape of the D=128 NeoX layout
 
 
 def _run_config(d, config):
@@ -146,8 +147,8 @@ def _run_config(d, config):
 @pytest.mark.parametrize("shape", [(4096, 32, 8, 8), (777, 5, 3, 2), (1, 16, 8, 8),
                                    (300, 64, 8, 8), (50, 100, 28, 3)])
 def test_launch_shapes_bit_identical(cuda_device, shape):
-    """The register-pipelined and the TMA-staged shapes share the row
-    arithmetic: every one gives the same bits."""
+    """The register-pipelined, one-shot general and TMA-staged shapes share
+    the row arithmetic and the lane mapping: every one gives the same bits."""
     assert [n.startswith("bulk") for n in kvq.configs("qk")] == [False] * 7 + [True] * 3
     T, Hq, Hk, Hv = shape
     d = wl.make_qk(T, Hq, Hk, Hv, theta=1e6, max_pos=131072, seed=T + Hq, device=cuda_device)
@@ -173,3 +174,43 @@ def test_staged_shape_finishing_from_global_memory(cuda_device, config):
     finally:
         kvq.set_qk_stage_wait_limit(old)
     assert kvq.set_qk_stage_wait_limit(old) == old
+
+
+def _run_layout(d, config):
+    out = d["qkv"].clone()
+    with with_config("qk", config):
+        kvq.fused_qk_norm_rope(out, d["Hq"], d["Hk"], d["Hv"], d["D"], d["eps"], d["q_weight"],
+                               d["k_weight"], d["cos_sin"], d["is_neox"], d["positions"],
+                               rotary_dim=d["rot"])
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("layout", [l for l in LAYOUTS if l[1] < l[0] or not l[2]],
+                         ids=lambda l: f"D{l[0]}_rot{l[1]}_{'neox' if l[2] else 'gptj'}")
+def test_general_staged_bit_identical(cuda_device, layout):
+    """The one-shot general kernel and every TMA-staged shape give the same
+    bits for every layout (shared row arithmetic and lane mapping)."""
+    D, rot, neox = layout
+    d = wl.make_qk(1500, 24, 8, 4, D=D, theta=1e6, max_pos=131072, seed=D * 3 + rot,
+                   device=cuda_device, rotary_dim=rot, is_neox=neox)
+    ref = _run_layout(d, 5)
+    for config in BULK:
+        assert torch.equal(_run_layout(d, config), ref), kvq.configs("qk")[config]
+
+
+@pytest.mark.parametrize("layout", [(64, 32, False), (256, 256, True), (256, 64, False)],
+                         ids=lambda l: f"D{l[0]}_rot{l[1]}_{'neox' if l[2] else 'gptj'}")
+def test_general_staged_finishing_from_global_memory(cuda_device, layout):
+    """Stage-wait limit 0 on the general layouts: every warp drains its copies
+    and finishes from global memory, with the same bits."""
+    D, rot, neox = layout
+    d = wl.make_qk(900, 16, 4, 4, D=D, theta=1e6, max_pos=131072, seed=D + rot + 1,
+                   device=cuda_device, rotary_dim=rot, is_neox=neox)
+    ref = _run_layout(d, 5)
+    old = kvq.set_qk_stage_wait_limit(0)
+    try:
+        for config in BULK:
+            assert torch.equal(_run_layout(d, config), ref), kvq.configs("qk")[config]
+    finally:
+        kvq.set_qk_stage_wait_limit(old)
