@@ -261,10 +261,17 @@ def _clone(d):
     return {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-@pytest.mark.parametrize("large", [False, True], ids=["decode", "prefill"])
-def test_cuda_graph_capture_and_replay(cuda_device, large):
+@pytest.mark.parametrize("large,qk_config", [(False, -1), (True, -1), (True, 7)],
+                         ids=["decode", "prefill", "prefill-qk-staged"])
+def test_cuda_graph_capture_and_replay(cuda_device, large, qk_config):
     """Both operators recorded into one CUDA graph (several layers) and
-    replayed twice give bit-identical results to the same calls run eagerly."""
+    replayed twice give bit-identical results to the same calls run eagerly
+    (also with the TMA-staged QK shape forced)."""
+    with with_config("qk", qk_config):
+        _graph_vs_eager(cuda_device, large)
+
+
+def _graph_vs_eager(cuda_device, large):
     T_qk, T_ds = (4096, 2048) if large else (17, 16)
     layers = [_layer_inputs(cuda_device, i, T_qk, T_ds) for i in range(4)]
     eager = [(_clone(qk), _clone(ds)) for qk, ds in layers]
