@@ -37,13 +37,18 @@
  *     or cudaHostRegister on a unified-addressing system).  On an
  *     NVLink-C2C coherent system (Grace-Blackwell) the kernels then read and
  *     write such host buffers directly over the interconnect, one pass, with
- *     no staging copy -- V of the packed QKV tensor never crosses it.  The
- *     library does not check which kind a pointer is.
+ *     no staging copy -- V of the packed QKV tensor never crosses it.  Only
+ *     the packed-QKV operator's large batches look at the kind: their
+ *     TMA-staged launch shapes copy qkv and cos_sin_cache with the bulk-copy
+ *     engine, so they are used only when both are device memory
+ *     (cudaPointerGetAttributes, one query per pointer and call); other
+ *     buffers take the register-pipelined shape, with the same results.
  *   - All buffers are owned by the caller.  The library allocates no memory,
  *     keeps no per-call state, and never synchronises the stream, so every
  *     entry point can be recorded into a CUDA graph (stream capture); call
- *     each operator once on the device before capturing, so that the one
- *     per-device occupancy query of the large-batch shapes is cached.
+ *     each operator once on the device before capturing, so that the
+ *     per-device set-up of the large-batch shapes (occupancy query, the
+ *     staged shapes' shared-memory opt-in) is done and cached.
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  A KVQ_OK
  *     return means "validated and enqueued"; kernel faults surface on the
  *     stream like any other kernel's.
