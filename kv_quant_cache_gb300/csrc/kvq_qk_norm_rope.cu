@@ -30,15 +30,13 @@
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 #include "kvq_qk_bulk.h"
-#include "kvq_qk_row.cuh"
+#include "kvq_qk_general_row.cuh"
 
 namespace kvq {
 namespace {
 
-using qk128::kHalf;
-using qk128::kHeadDim;
-using qk128::row_math;
-using QkWeights = qk128::Weights;
+constexpr int kHeadDim = 128;
+constexpr int kHalf = kHeadDim / 2;
 
 struct QkParams {
   __nv_bfloat16* qkv;
@@ -57,6 +55,35 @@ struct QkParams {
   int64_t max_pos;    // bounds-checked launches: rows of cos_sin
   int* errors;        // bounds-checked launches: tokens rejected
 };
+
+// Weight fragments of this lane (dims [4l, 4l+4) and [64+4l, 64+4l+4), Q and
+// K), kept packed as bf16 and widened where they are used.
+struct QkWeights {
+  uint2 q_lo, q_hi, k_lo, k_hi;
+};
+
+__device__ __forceinline__ void load_weights(const QkParams& p, int l16, QkWeights& w) {
+  const uint2* q = reinterpret_cast<const uint2*>(p.q_weight);
+  const uint2* k = reinterpret_cast<const uint2*>(p.k_weight);
+  w.q_lo = __ldg(q + l16);
+  w.q_hi = __ldg(q + 16 + l16);
+  w.k_lo = __ldg(k + l16);
+  w.k_hi = __ldg(k + 16 + l16);
+}
+
+// Normalise + rotate one row fragment; all 32 lanes must call it together
+// (the sum of squares is reduced across the half-warp).  The arithmetic is
+// that of every layout (kvq_qk_general_row.cuh) at head_dim 128, NeoX, full
+// rotation, whose lane geometry is this kernel's: every launch shape of the
+// operator gives the same bits.
+__device__ __forceinline__ void row_math(uint2& lo, uint2& hi, bool is_q, const QkWeights& w,
+                                         const float4& c4, const float4& s4, float eps) {
+  const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+  const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+  const qkgen::Lane<kHeadDim, 4, true> full(0, kHeadDim);  // both fragments rotated
+  qkgen::row_math<kHeadDim, 4, true>(lo, hi, is_q ? w.q_lo : w.k_lo, is_q ? w.q_hi : w.k_hi, c, s,
+                                     full, eps);
+}
 
 // The lane's 4 cosines and 4 sines of the token's row.
 __device__ __forceinline__ void load_cos_sin(const QkParams& p, int t, int l16, float4& c,
@@ -153,7 +180,7 @@ qk_tiles_kernel(const QkParams p) {
   const int item = blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (item >= p.items) return;  // whole warp leaves together
   QkWeights w;
-  qk128::load_weights(p.q_weight, p.k_weight, lane & 15, w);
+  load_weights(p, lane & 15, w);
   do_item<STEPS, CHECKED>(p, item, lane >> 4, lane & 15, w);
 }
 
@@ -165,7 +192,7 @@ qk_stream_kernel(const QkParams p) {
   const int nw = gridDim.x * WARPS;
   if (gw >= p.items) return;
   QkWeights w;
-  qk128::load_weights(p.q_weight, p.k_weight, lane & 15, w);
+  load_weights(p, lane & 15, w);
   for (int item = gw; item < p.items; item += nw) do_item<STEPS>(p, item, lane >> 4, lane & 15, w);
 }
 
