@@ -598,6 +598,17 @@ def sweep(kvq, device):
         emit({"sweep": "qk_dispatch", "T": T, "rows": T * 40, "bytes": nb, "us": res,
               "auto": names[kvq.qk_config_for(T, 32, 8)]})
         del d
+    # the copy ceiling by launch length: a device copy moving (read + write)
+    # the given traffic, for comparison with any kernel of the same bytes
+    for mb in (64, 128, 256, 512, 1024, 2048, 4096, 8192):
+        src = torch.empty(mb * 2**19, dtype=torch.uint8, device=device)
+        dst = torch.empty_like(src)
+        med, _ = _time_launch(lambda: dst.copy_(src), 20, stream,
+                              flush if mb < 256 else None)
+        emit({"sweep": "d2d_copy_ceiling", "traffic_mb": mb, "us_median": round(med * 1e3, 2),
+              "gbs": round(mb * 2**20 / med / 1e6, 1),
+              "pct_peak": round(100 * mb * 2**20 / med / 1e6 / peak, 1)})
+        del src, dst
     # a copy moving the QK step's bytes (Q+K rows read and written): the
     # ceiling for a launch of that length
     nb = qk_bytes(wl.QK_LARGE.T, wl.QK_LARGE.Hq, wl.QK_LARGE.Hk)

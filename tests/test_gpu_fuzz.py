@@ -23,7 +23,12 @@ def _qk_cases(n=40, seed=2024):
         Hq, Hk, Hv = (int(x) for x in rng.integers(0, 9, size=3))
         if Hq + Hk == 0:
             Hq = 1
-        forced = int(rng.integers(-1, len(kvq.configs("qk")))) if (D, rot, neox) == (128, 128, True) else -1
+        # every shape for the head_dim-128 full-NeoX layout; otherwise the
+        # automatic choice, the one-shot general kernel or a staged shape
+        names = kvq.configs("qk")
+        choices = [-1] + [c for c, n in enumerate(names)
+                          if (D, rot, neox) == (128, 128, True) or n.startswith(("general", "bulk"))]
+        forced = int(rng.choice(choices))
         out.append((i, T, Hq, Hk, Hv, D, rot, neox, forced))
     return out
 
