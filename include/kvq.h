@@ -291,20 +291,21 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  *   *_config_for    the configuration a call with these sizes would use now
  */
 /*
- * Staged QK launch shapes (configurations named bulk<...>): each warp keeps
- * its next items in flight in shared memory through the bulk-copy (TMA)
- * engine and waits on an mbarrier per stage.  Every such wait polls at most
- * `polls` times (default 1 << 22) and for at most 20 ms.  A warp whose wait
- * runs out lets its copies in flight land (each wait bounded again), then
- * finishes its remaining rows from global memory, with the same results: the
- * limit bounds how long a stalled copy can hold a warp and never changes an
- * output.  0 sends every staged launch straight to that path (diagnostics and
- * tests).  Applies to launches enqueued after the call; returns the previous
- * limit.  Not synchronised with launches on other threads.  The staged shapes
- * serve only qkv and cos/sin tables in device memory; other buffers take the
+ * Staged launch shapes (the packed-QKV operator's configurations named
+ * bulk<...>): each warp keeps its next items in flight in shared memory
+ * through the bulk-copy (TMA) engine and waits on an mbarrier per stage.
+ * Every such wait polls at most `polls` times (default 1 << 22) and for at
+ * most 20 ms.  A warp whose wait runs out lets its copies in flight land
+ * (each wait bounded again), then finishes its remaining rows from global
+ * memory, with the same results: the limit bounds how long a stalled copy can
+ * hold a warp and never changes an output.  0 sends every staged launch
+ * straight to that path (diagnostics and tests).  Applies to launches
+ * enqueued after the call; returns the previous limit.  Not synchronised
+ * with launches on other threads.  The staged shapes copy only from device
+ * memory (qkv and the cos/sin table); other buffers take the
  * register-pipelined large-batch shape.
  */
-uint32_t kvq_set_qk_stage_wait_limit(uint32_t polls);
+uint32_t kvq_set_stage_wait_limit(uint32_t polls);
 
 int kvq_qk_num_configs(void);
 const char* kvq_qk_config_name(int id);

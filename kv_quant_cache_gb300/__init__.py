@@ -85,8 +85,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         getattr(L, f"kvq_set_{op}_config").argtypes = [_I]
     L.kvq_qk_config_for.restype = _I
     L.kvq_qk_config_for.argtypes = [_I64, _I, _I]
-    L.kvq_set_qk_stage_wait_limit.restype = ctypes.c_uint32
-    L.kvq_set_qk_stage_wait_limit.argtypes = [ctypes.c_uint32]
+    L.kvq_set_stage_wait_limit.restype = ctypes.c_uint32
+    L.kvq_set_stage_wait_limit.argtypes = [ctypes.c_uint32]
     L.kvq_dsv4_config_for.restype = _I
     L.kvq_dsv4_config_for.argtypes = [_I64, _I]
     return L
@@ -266,10 +266,10 @@ def set_config(op: str, config_id: int) -> int:
     return prev
 
 
-def set_qk_stage_wait_limit(polls: int) -> int:
-    """Polls of a stage barrier before a staged QK warp finishes from global
-    memory (0: always); returns the previous limit."""
-    return lib().kvq_set_qk_stage_wait_limit(int(polls))
+def set_stage_wait_limit(polls: int) -> int:
+    """Polls of a stage barrier before a warp of a staged QK launch shape
+    finishes from global memory (0: always); returns the previous limit."""
+    return lib().kvq_set_stage_wait_limit(int(polls))
 
 
 def qk_config_for(num_tokens: int, num_heads_q: int, num_heads_k: int) -> int:

@@ -8,6 +8,7 @@
 #include "kvq.h"
 #include "kvq_launch.h"
 #include "kvq_qk_bulk.h"
+#include "kvq_tma.cuh"
 
 namespace {
 
@@ -98,6 +99,16 @@ int set_config(std::atomic<int>& slot, int id, int n) {
 }  // namespace
 
 namespace kvq {
+
+namespace {
+std::atomic<uint32_t> g_stage_wait_limit{1u << 22};
+}  // namespace
+
+uint32_t stage_wait_limit() { return g_stage_wait_limit.load(std::memory_order_relaxed); }
+
+uint32_t set_stage_wait_limit(uint32_t polls) {
+  return g_stage_wait_limit.exchange(polls, std::memory_order_relaxed);
+}
 
 int device_sm_count() {
   int dev = 0;
@@ -350,7 +361,7 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
   return num_tokens * (int64_t)(num_heads + 1) < current_threshold() ? 0 : 1;
 }
 
-uint32_t kvq_set_qk_stage_wait_limit(uint32_t polls) { return kvq::set_qk_stage_wait_limit(polls); }
+uint32_t kvq_set_stage_wait_limit(uint32_t polls) { return kvq::set_stage_wait_limit(polls); }
 
 int kvq_qk_num_configs(void) { return kvq::kQkNumConfigs; }
 

@@ -37,6 +37,7 @@
 #include "kvq_launch.h"
 #include "kvq_qk_bulk.h"
 #include "kvq_qk_general_row.cuh"
+#include "kvq_tma.cuh"
 
 namespace kvq {
 namespace {
@@ -45,12 +46,7 @@ using qkgen::Lane;
 using Frag4 = qkgen::Frag<4>;
 constexpr int kF = 4;                    // dims per fragment
 constexpr int kUnroll = 4;               // row steps computed together
-constexpr uint32_t kDefaultWaitLimit = 1u << 22;
-constexpr uint64_t kWaitNs = 20000000;   // 20 ms: a stage wait then gives up
-constexpr uint32_t kDrainPolls = 1u << 22;
-constexpr uint64_t kDrainNs = 100000000; // 100 ms per copy still in flight
-
-std::atomic<uint32_t> g_wait_limit{kDefaultWaitLimit};
+using namespace tma;
 
 struct BulkParams {
   __nv_bfloat16* qkv;
@@ -68,85 +64,6 @@ struct BulkParams {
   float eps;
   uint32_t wait_limit;
 };
-
-// ---- inline PTX: mbarrier, bulk copy, cache policy, proxy fence, timer -----
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Makes initialised barriers visible to the bulk-copy engine.
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// One arrival that also announces `bytes` of copies completing on the barrier.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Polls the completion of the barrier phase with parity `parity` at most
-// `limit` times and for about `ns` nanoseconds at most (the clock is read
-// every 64 polls); the result is the same on every lane of the warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t limit,
-                                               uint64_t ns) {
-  bool done = limit > 0 && mbar_test(bar, parity);
-  if (!done && limit > 1) {
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1; i < limit; ++i) {
-      if ((done = mbar_test(bar, parity))) break;
-      if ((i & 63u) == 0 && global_ns() - t0 > ns) break;
-    }
-  }
-  return __all_sync(kFullMask, done);
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// Global -> shared bulk copy completing on `bar` (addresses 16-byte aligned,
-// size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(__cvta_generic_to_global(src)), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
-}
-
-// Orders this thread's earlier shared-memory accesses before later
-// bulk-copy writes to the same stage.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // ---- work items -------------------------------------------------------------
 
@@ -312,35 +229,6 @@ constexpr size_t smem_bytes() {
   return (size_t)WARPS * NS * (STAGE_BYTES + 4 * D) + (size_t)WARPS * NS * 8;
 }
 
-// Opts the kernel in to its shared memory and counts its resident CTAs per
-// SM, once per device.
-template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
-cudaError_t prepare(int* per_sm) {
-  static std::atomic<int> cache[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const bool cached = dev >= 0 && dev < kMaxDevices;
-  if (cached) {
-    const int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) {
-      *per_sm = v;
-      return cudaSuccess;
-    }
-  }
-  auto kernel = qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>;
-  constexpr size_t bytes = smem_bytes<D, WARPS, NS, STAGE_BYTES>();
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, WARPS * 32, bytes);
-  if (e != cudaSuccess) return e;
-  if (n < 1) return cudaErrorInvalidConfiguration;
-  if (cached) cache[dev].store(n, std::memory_order_relaxed);
-  *per_sm = n;
-  return cudaSuccess;
-}
-
 void chunking(const QkArgs& a, int rmax, int* chunks, int* chunk_rows) {
   const int rows = a.num_heads_q + a.num_heads_k;
   *chunks = (rows + rmax - 1) / rmax;
@@ -350,8 +238,10 @@ void chunking(const QkArgs& a, int rmax, int* chunks, int* chunk_rows) {
 template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
 cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   static_assert(smem_bytes<D, WARPS, NS, STAGE_BYTES>() <= 227 * 1024, "shared memory per CTA");
+  static std::atomic<int> cache[kMaxDevices];
   int per_sm = 0;
-  cudaError_t e = prepare<D, NEOX, WARPS, NS, STAGE_BYTES>(&per_sm);
+  cudaError_t e = prepare(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>, WARPS * 32,
+                          smem_bytes<D, WARPS, NS, STAGE_BYTES>(), cache, &per_sm);
   if (e != cudaSuccess) return e;
   BulkParams p;
   p.qkv = static_cast<__nv_bfloat16*>(a.qkv);
@@ -366,7 +256,7 @@ cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   chunking(a, STAGE_BYTES / (2 * D), &p.chunks, &p.chunk_rows);
   p.items = a.num_tokens * p.chunks;
   p.eps = a.eps;
-  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.wait_limit = stage_wait_limit();
   int64_t grid = (int64_t)per_sm * device_sm_count();
   const int64_t need = (p.items + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
@@ -391,15 +281,6 @@ cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
                   : launch_layout<256, false, WARPS, NS, STAGE_BYTES>(a, stream);
   }
   return cudaErrorInvalidValue;
-}
-
-bool device_memory(const void* ptr) {
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();  // a failed query is not sticky: clear it before the launch
-    return false;
-  }
-  return attr.type == cudaMemoryTypeDevice;
 }
 
 }  // namespace
@@ -427,10 +308,6 @@ cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream) {
   };
   if (shape < 0 || shape >= kQkBulkShapes) return cudaErrorInvalidValue;
   return kLaunch[shape](a, stream);
-}
-
-uint32_t set_qk_stage_wait_limit(uint32_t polls) {
-  return g_wait_limit.exchange(polls, std::memory_order_relaxed);
 }
 
 }  // namespace kvq

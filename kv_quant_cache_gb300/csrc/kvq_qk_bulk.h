@@ -29,8 +29,4 @@ bool qk_bulk_eligible(const QkArgs& a, int shape);
 // layout (head_dim 64 / 128 / 256, NeoX or GPT-J, full or partial rotation).
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream);
 
-// Polls of a stage barrier after which a warp stops staging and finishes its
-// items with direct loads (default 1 << 22).  Returns the previous value.
-uint32_t set_qk_stage_wait_limit(uint32_t polls);
-
 }  // namespace kvq

@@ -25,8 +25,8 @@ def test_decode_size_16_tokens(cuda_device, threshold):
 
 
 def test_prefill_32768x64_every_token(cuda_device):
-    """The benchmarked workload (default dispatch = token-tiled launch), every
-    token and the whole cache compared."""
+    """The benchmarked workload (default dispatch = the persistent launch),
+    every token and the whole cache compared."""
     d = wl.make_dsv4_workload(wl.DSV4_LARGE, device=cuda_device)
     assert kvq.dsv4_dispatch_path(32768, 64) == 1
     qrep, crep = dsv4_parity(d, slice_tokens=1024)
@@ -154,6 +154,31 @@ def test_every_launch_config(cuda_device, config, shape):
         dsv4_parity(d)
 
 
+def _dsv4_run_config(d, config):
+    q = d["q"].clone()
+    cache = d["kv_cache"].clone()
+    with with_config("dsv4", config):
+        kvq.dsv4_qnorm_rope_kv_rope_quant_insert(q, d["kv"], d["eps"], d["q_weight"],
+                                                 d["kv_weight"], d["cos_sin"], d["positions"],
+                                                 d["slot_mapping"], cache)
+    torch.cuda.synchronize()
+    return q, cache
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (17, 3), (300, 7), (2048, 64), (513, 128)])
+def test_launch_shapes_bit_identical(cuda_device, shape):
+    """Every launch shape (one-shot, persistent) shares the row arithmetic: q
+    and the whole cache come out as the same bytes."""
+    T, H = shape
+    d = wl.make_dsv4(T, H, max_pos=131072, num_blocks=-(-2 * T // 16), block_size=16,
+                     slots="distinct_skip2", seed=400 + T + H, device=cuda_device)
+    q_ref, c_ref = _dsv4_run_config(d, 4)
+    assert not torch.equal(q_ref, d["q"])
+    for config in DSV4_CONFIGS:
+        q, c = _dsv4_run_config(d, config)
+        assert torch.equal(q, q_ref) and torch.equal(c, c_ref), kvq.configs("dsv4")[config]
+
+
 # ---- reading entries back (dsv4_kv_cache_gather) ---------------------------
 
 def _gather_vs_oracle(cache_dev, slots):
@@ -261,13 +286,13 @@ def _clone(d):
     return {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-@pytest.mark.parametrize("large,qk_config", [(False, -1), (True, -1), (True, 7)],
-                         ids=["decode", "prefill", "prefill-qk-staged"])
-def test_cuda_graph_capture_and_replay(cuda_device, large, qk_config):
+@pytest.mark.parametrize("large,staged", [(False, False), (True, False), (True, True)],
+                         ids=["decode", "prefill", "prefill-staged"])
+def test_cuda_graph_capture_and_replay(cuda_device, large, staged):
     """Both operators recorded into one CUDA graph (several layers) and
     replayed twice give bit-identical results to the same calls run eagerly
     (also with the TMA-staged QK shape forced)."""
-    with with_config("qk", qk_config):
+    with with_config("qk", 7 if staged else -1):
         _graph_vs_eager(cuda_device, large)
 
 

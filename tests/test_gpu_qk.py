@@ -165,15 +165,15 @@ def test_staged_shape_finishing_from_global_memory(cuda_device, config):
     direct loads.  The results are the same bits, and match the oracle."""
     d = wl.make_qk(2000, 32, 8, 8, theta=1e6, max_pos=131072, seed=61, device=cuda_device)
     ref = _run_config(d, 2)
-    old = kvq.set_qk_stage_wait_limit(0)
+    old = kvq.set_stage_wait_limit(0)
     try:
         assert old > 0
         assert torch.equal(_run_config(d, config), ref)
         with with_config("qk", config):
             qk_parity(d)
     finally:
-        kvq.set_qk_stage_wait_limit(old)
-    assert kvq.set_qk_stage_wait_limit(old) == old
+        kvq.set_stage_wait_limit(old)
+    assert kvq.set_stage_wait_limit(old) == old
 
 
 def _run_layout(d, config):
@@ -208,9 +208,9 @@ def test_general_staged_finishing_from_global_memory(cuda_device, layout):
     d = wl.make_qk(900, 16, 4, 4, D=D, theta=1e6, max_pos=131072, seed=D + rot + 1,
                    device=cuda_device, rotary_dim=rot, is_neox=neox)
     ref = _run_layout(d, 5)
-    old = kvq.set_qk_stage_wait_limit(0)
+    old = kvq.set_stage_wait_limit(0)
     try:
         for config in BULK:
             assert torch.equal(_run_layout(d, config), ref), kvq.configs("qk")[config]
     finally:
-        kvq.set_qk_stage_wait_limit(old)
+        kvq.set_stage_wait_limit(old)
