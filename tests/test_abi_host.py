@@ -260,3 +260,14 @@ def test_checked_entry_points_validation(L):
     assert L.dsv4_kv_cache_gather_checked(A16, 8, 64, A16, 4, A16, None, None) == kvq.KVQ_ERR_NULL
     assert L.dsv4_kv_cache_gather_checked(A16, -1, 64, A16, 4, A16, E, None) == kvq.KVQ_ERR_SHAPE
     assert L.dsv4_kv_cache_gather_checked(A16, 8, 64, A16, 4, A16 + 8, E, None) == kvq.KVQ_ERR_ALIGN
+
+
+def test_stage_wait_limit_round_trip(L):
+    """The staged shapes' wait limit: returns the previous value, default 2^22."""
+    old = kvq.set_stage_wait_limit(17)
+    try:
+        assert old == 1 << 22
+        assert kvq.set_stage_wait_limit(0) == 17
+        assert kvq.set_stage_wait_limit(5) == 0
+    finally:
+        assert kvq.set_stage_wait_limit(old) == 5
