@@ -682,20 +682,42 @@ def sweep(kvq, device):
         for qk, ds in layers:
             launch_qk(kvq, qk, st)
             launch_dsv4(kvq, ds, st)
-    decode_step(stream)
-    torch.cuda.synchronize()
-    eager_ms, _ = _time_launch(lambda: decode_step(stream), 20, stream)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        decode_step(torch.cuda.current_stream(device))
-    graph.replay()
-    torch.cuda.synchronize()
-    graph_ms, _ = _time_launch(graph.replay, 20, stream)
-    emit({"sweep": "decode_32_layers", "eager_us": round(eager_ms * 1e3, 1),
-          "graph_us": round(graph_ms * 1e3, 1),
-          "eager_us_per_launch": round(eager_ms * 1e3 / 64, 2),
-          "graph_us_per_launch": round(graph_ms * 1e3 / 64, 2)})
-    del layers, graph
+    for pdl in (False, True):
+        old = kvq.set_programmatic_launch(pdl)
+        try:
+            decode_step(stream)
+            torch.cuda.synchronize()
+            eager_ms, _ = _time_launch(lambda: decode_step(stream), 20, stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                decode_step(torch.cuda.current_stream(device))
+            graph.replay()
+            torch.cuda.synchronize()
+            graph_ms, _ = _time_launch(graph.replay, 20, stream)
+        finally:
+            kvq.set_programmatic_launch(old)
+        emit({"sweep": "decode_32_layers", "programmatic_launch": pdl,
+              "eager_us": round(eager_ms * 1e3, 1), "graph_us": round(graph_ms * 1e3, 1),
+              "eager_us_per_launch": round(eager_ms * 1e3 / 64, 2),
+              "graph_us_per_launch": round(graph_ms * 1e3 / 64, 2)})
+        del graph
+    del layers
+    # the benchmarked step with and without programmatic dependent launch
+    qk, ds = make_step_inputs(device)
+    nb = sum(step_bytes(qk, ds))
+    for pdl in (False, True):
+        old = kvq.set_programmatic_launch(pdl)
+        try:
+            def step():
+                launch_qk(kvq, qk, stream)
+                launch_dsv4(kvq, ds, stream)
+            step()
+            med, _ = _time_launch(step, 50, stream)
+        finally:
+            kvq.set_programmatic_launch(old)
+        emit({"sweep": "step", "programmatic_launch": pdl, "us_median": round(med * 1e3, 2),
+              "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1)})
+    del qk, ds
     # dispatch crossover between the small- and large-batch shapes
     for H in (64, 128):
         for T in (1, 4, 16, 64, 128, 256, 512, 1024, 4096):

@@ -307,6 +307,21 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  */
 uint32_t kvq_set_stage_wait_limit(uint32_t polls);
 
+/*
+ * Programmatic dependent launch.  enable != 0: later launches of this library
+ * carry CUDA's programmatic stream serialization attribute, so a kernel may be
+ * scheduled while the kernel before it on the stream is still finishing.
+ * Every kernel of this library first waits until the kernels it depends on
+ * have completed and their writes are visible (griddepcontrol.wait), then
+ * lets the next kernel be scheduled; results and stream order are those of
+ * ordinary launches, and only the launch gaps shrink (short, launch-bound
+ * calls such as decode steps, also inside CUDA graphs).  Default off.
+ * Returns the previous setting (0 or 1).  Not synchronised with launches on
+ * other threads.  No counterpart in the source pages: a launch option of this
+ * library.
+ */
+int kvq_set_programmatic_launch(int enable);
+
 int kvq_qk_num_configs(void);
 const char* kvq_qk_config_name(int id);
 int kvq_set_qk_config(int id);

@@ -87,6 +87,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.kvq_qk_config_for.argtypes = [_I64, _I, _I]
     L.kvq_set_stage_wait_limit.restype = ctypes.c_uint32
     L.kvq_set_stage_wait_limit.argtypes = [ctypes.c_uint32]
+    L.kvq_set_programmatic_launch.restype = _I
+    L.kvq_set_programmatic_launch.argtypes = [_I]
     L.kvq_dsv4_config_for.restype = _I
     L.kvq_dsv4_config_for.argtypes = [_I64, _I]
     return L
@@ -270,6 +272,13 @@ def set_stage_wait_limit(polls: int) -> int:
     """Polls of a stage barrier before a warp of a staged QK launch shape
     finishes from global memory (0: always); returns the previous limit."""
     return lib().kvq_set_stage_wait_limit(int(polls))
+
+
+def set_programmatic_launch(enable: bool) -> bool:
+    """Launch later kernels with programmatic stream serialization (they may be
+    scheduled while the previous kernel finishes; results are unchanged);
+    returns the previous setting."""
+    return bool(lib().kvq_set_programmatic_launch(1 if enable else 0))
 
 
 def qk_config_for(num_tokens: int, num_heads_q: int, num_heads_k: int) -> int:

@@ -102,7 +102,10 @@ namespace kvq {
 
 namespace {
 std::atomic<uint32_t> g_stage_wait_limit{1u << 22};
+std::atomic<bool> g_programmatic_launch{false};
 }  // namespace
+
+bool programmatic_launch() { return g_programmatic_launch.load(std::memory_order_relaxed); }
 
 uint32_t stage_wait_limit() { return g_stage_wait_limit.load(std::memory_order_relaxed); }
 
@@ -362,6 +365,10 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
 }
 
 uint32_t kvq_set_stage_wait_limit(uint32_t polls) { return kvq::set_stage_wait_limit(polls); }
+
+int kvq_set_programmatic_launch(int enable) {
+  return kvq::g_programmatic_launch.exchange(enable != 0, std::memory_order_relaxed) ? 1 : 0;
+}
 
 int kvq_qk_num_configs(void) { return kvq::kQkNumConfigs; }
 

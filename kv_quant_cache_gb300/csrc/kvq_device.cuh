@@ -48,6 +48,15 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch.  Every kernel starts with both: it waits
+// until the grids it depends on have completed and their writes are visible
+// (a no-op when it was launched the ordinary way), then lets the next grid on
+// the stream be scheduled while it runs.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 16-byte accesses for data touched exactly once (evict-first).
 __device__ __forceinline__ uint4 load_stream(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));

@@ -240,6 +240,7 @@ __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, cons
 template <int WARPS, int QROWS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_tiles_kernel(const Dsv4Params p) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if ((int)blockIdx.x < p.kv_ctas) {
@@ -307,6 +308,7 @@ __device__ __forceinline__ void stream_q(const Dsv4Params& p, int gw, int nw, in
 template <int WARPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_stream_kernel(const Dsv4Params p) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = (int)gridDim.x * WARPS;
@@ -341,9 +343,8 @@ cudaError_t launch_tiles(const Dsv4Args& a, cudaStream_t stream) {
   Dsv4Params p = make_params(a);
   p.kv_ctas = (p.num_tokens + WARPS - 1) / WARPS;
   const int q_ctas = (p.q_rows + WARPS * QROWS - 1) / (WARPS * QROWS);
-  dsv4_tiles_kernel<WARPS, QROWS, MINB, CHECKED>
-      <<<p.kv_ctas + q_ctas, WARPS * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(dsv4_tiles_kernel<WARPS, QROWS, MINB, CHECKED>,
+                       dim3((unsigned)(p.kv_ctas + q_ctas)), dim3(WARPS * 32), 0, stream, p);
 }
 
 template <int WARPS, int MINB, bool CHECKED = false>
@@ -357,8 +358,8 @@ cudaError_t launch_stream(const Dsv4Args& a, cudaStream_t stream) {
   const int64_t need = (work_warps + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  dsv4_stream_kernel<WARPS, MINB, CHECKED><<<(unsigned)grid, WARPS * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(dsv4_stream_kernel<WARPS, MINB, CHECKED>, dim3((unsigned)grid),
+                       dim3(WARPS * 32), 0, stream, p);
 }
 
 }  // namespace

@@ -64,6 +64,7 @@ __device__ __forceinline__ uint4 dequant8(const uint2 codes, float scale) {
 template <bool CHECKED>
 __global__ void __launch_bounds__(kWarps * 32)
 dsv4_gather_kernel(const GatherParams p) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (row >= p.num_rows) return;  // whole warp leaves together
@@ -110,9 +111,8 @@ cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream) {
   p.num_slots = a.num_slots;
   p.errors = a.errors;
   const unsigned grid = (unsigned)((p.num_rows + kWarps - 1) / kWarps);
-  if (a.errors != nullptr) dsv4_gather_kernel<true><<<grid, kWarps * 32, 0, stream>>>(p);
-  else dsv4_gather_kernel<false><<<grid, kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(a.errors != nullptr ? dsv4_gather_kernel<true> : dsv4_gather_kernel<false>,
+                       dim3(grid), dim3(kWarps * 32), 0, stream, p);
 }
 
 }  // namespace kvq

@@ -73,6 +73,34 @@ cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream);
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
+// Programmatic dependent launch (kvq_set_programmatic_launch).  When on,
+// kernels are launched with programmatic stream serialization: a kernel may
+// be scheduled while the previous kernel on the stream is finishing, and
+// every kernel of this library waits for that kernel's completion before its
+// first memory access (grid_dependency_sync), so results and stream order are
+// those of an ordinary launch.
+bool programmatic_launch();
+
+// Launches `kernel` with one by-value parameter block; the launch error is
+// returned (and cleared).
+template <typename Params>
+cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+  const cudaError_t last = cudaGetLastError();
+  return e != cudaSuccess ? e : last;
+}
+
 constexpr int kMaxDevices = 64;
 
 // CTAs of `kernel` that fit on one SM at `threads` threads per CTA, cached

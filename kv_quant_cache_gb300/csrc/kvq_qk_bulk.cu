@@ -136,6 +136,7 @@ __device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, i
 template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 qk_bulk_kernel(const BulkParams p) {
+  grid_dependency_sync();
   constexpr int kCsAt = STAGE_BYTES;           // cos/sin row inside a stage
   constexpr int kStage = STAGE_BYTES + 4 * D;  // room for a full-width cos/sin row
   constexpr int LPR = D / (2 * kF);            // lanes per row
@@ -261,9 +262,8 @@ cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   const int64_t need = (p.items + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>
-      <<<(unsigned)grid, WARPS * 32, smem_bytes<D, WARPS, NS, STAGE_BYTES>(), stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>, dim3((unsigned)grid),
+                       dim3(WARPS * 32), smem_bytes<D, WARPS, NS, STAGE_BYTES>(), stream, p);
 }
 
 template <int WARPS, int NS, int STAGE_BYTES>

@@ -46,6 +46,7 @@ using qkgen::Lane;
 template <int D, int F, int STEPS, bool NEOX, bool CHECKED>
 __global__ void __launch_bounds__(128)
 qk_general_kernel(const GenParams p) {
+  grid_dependency_sync();
   using V = typename Frag<F>::T;
   constexpr int LPR = D / (2 * F);  // lanes per row
   constexpr int RPW = 32 / LPR;     // rows per warp step
@@ -127,8 +128,8 @@ cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
   p.steps = (groups + p.chunks - 1) / p.chunks;
   p.items = a.num_tokens * p.chunks;
   const unsigned grid = (unsigned)((p.items + 3) / 4);
-  qk_general_kernel<D, F, STEPS, NEOX, CHECKED><<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(qk_general_kernel<D, F, STEPS, NEOX, CHECKED>, dim3(grid), dim3(128), 0,
+                       stream, p);
 }
 
 // Small batches: one warp step per item (widest spread); large batches: up to

@@ -176,6 +176,7 @@ __device__ __forceinline__ void do_item(const QkParams& p, int item, int half, i
 template <int WARPS, int STEPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 qk_tiles_kernel(const QkParams p) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (item >= p.items) return;  // whole warp leaves together
@@ -187,6 +188,7 @@ qk_tiles_kernel(const QkParams p) {
 template <int WARPS, int STEPS, int MINB>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 qk_stream_kernel(const QkParams p) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
@@ -222,8 +224,8 @@ template <int WARPS, int STEPS, int MINB, bool CHECKED = false>
 cudaError_t launch_tiles(const QkArgs& a, cudaStream_t stream) {
   const QkParams p = make_params(a, STEPS);
   const unsigned grid = (unsigned)((p.items + WARPS - 1) / WARPS);
-  qk_tiles_kernel<WARPS, STEPS, MINB, CHECKED><<<grid, WARPS * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(qk_tiles_kernel<WARPS, STEPS, MINB, CHECKED>, dim3(grid), dim3(WARPS * 32),
+                       0, stream, p);
 }
 
 template <typename Kernel>
@@ -235,8 +237,7 @@ cudaError_t launch_persistent(Kernel kernel, const QkParams& p, int warps, cudaS
   const int64_t need = (p.items + warps - 1) / warps;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, warps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)grid), dim3(warps * 32), 0, stream, p);
 }
 
 template <int WARPS, int STEPS, int MINB>

@@ -271,3 +271,13 @@ def test_stage_wait_limit_round_trip(L):
         assert kvq.set_stage_wait_limit(5) == 0
     finally:
         assert kvq.set_stage_wait_limit(old) == 5
+
+
+def test_programmatic_launch_switch(L):
+    old = kvq.set_programmatic_launch(True)
+    try:
+        assert old is False
+        assert kvq.set_programmatic_launch(False) is True
+        assert kvq.set_programmatic_launch(True) is False
+    finally:
+        kvq.set_programmatic_launch(old)

@@ -286,14 +286,54 @@ def _clone(d):
     return {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-@pytest.mark.parametrize("large,staged", [(False, False), (True, False), (True, True)],
-                         ids=["decode", "prefill", "prefill-staged"])
-def test_cuda_graph_capture_and_replay(cuda_device, large, staged):
+@pytest.mark.parametrize("large,staged,pdl", [(False, False, False), (True, False, False),
+                                              (True, True, False), (False, False, True),
+                                              (True, True, True)],
+                         ids=["decode", "prefill", "prefill-staged", "decode-pdl",
+                              "prefill-staged-pdl"])
+def test_cuda_graph_capture_and_replay(cuda_device, large, staged, pdl):
     """Both operators recorded into one CUDA graph (several layers) and
     replayed twice give bit-identical results to the same calls run eagerly
-    (also with the TMA-staged QK shape forced)."""
+    (also with the TMA-staged QK shape forced, and with programmatic
+    dependent launch on)."""
+    old = kvq.set_programmatic_launch(pdl)
+    try:
+        with with_config("qk", 7 if staged else -1):
+            _graph_vs_eager(cuda_device, large)
+    finally:
+        kvq.set_programmatic_launch(old)
+
+
+@pytest.mark.parametrize("staged", [False, True], ids=["tiles", "staged"])
+def test_programmatic_launch_keeps_dependencies(cuda_device, staged):
+    """With programmatic dependent launch on, kernels that read what the
+    previous kernel on the stream wrote still see it: the packed-QKV operator
+    applied twice to the same tensor, then an insert followed by a gather of
+    the entries it wrote, give the bytes of ordinary launches."""
+    qk = wl.make_qk(8192, 32, 8, 8, theta=1e6, max_pos=131072, seed=71, device=cuda_device)
+    ds = wl.make_dsv4(2048, 64, max_pos=131072, num_blocks=64, block_size=64, seed=72,
+                      device=cuda_device)
+
+    def chain():
+        a, b = _clone(qk), _clone(ds)
+        for _ in range(3):
+            kvq.fused_qk_norm_rope(a["qkv"], 32, 8, 8, 128, a["eps"], a["q_weight"],
+                                   a["k_weight"], a["cos_sin"], True, a["positions"])
+        run_dsv4(b)
+        rows = kvq.dsv4_kv_cache_gather(b["kv_cache"], b["slot_mapping"])
+        run_dsv4(b)
+        torch.cuda.synchronize()
+        return a["qkv"], b["q"], b["kv_cache"], rows
+
     with with_config("qk", 7 if staged else -1):
-        _graph_vs_eager(cuda_device, large)
+        ref = chain()
+        old = kvq.set_programmatic_launch(True)
+        try:
+            got = chain()
+        finally:
+            kvq.set_programmatic_launch(old)
+    for x, y in zip(ref, got):
+        assert torch.equal(x, y)
 
 
 def _graph_vs_eager(cuda_device, large):
