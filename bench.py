@@ -702,22 +702,28 @@ def sweep(kvq, device):
               "graph_us_per_launch": round(graph_ms * 1e3 / 64, 2)})
         del graph
     del layers
-    # the benchmarked step with and without programmatic dependent launch
-    qk, ds = make_step_inputs(device)
-    nb = sum(step_bytes(qk, ds))
-    for pdl in (False, True):
-        old = kvq.set_programmatic_launch(pdl)
-        try:
-            def step():
-                launch_qk(kvq, qk, stream)
-                launch_dsv4(kvq, ds, stream)
-            step()
-            med, _ = _time_launch(step, 50, stream)
-        finally:
-            kvq.set_programmatic_launch(old)
-        emit({"sweep": "step", "programmatic_launch": pdl, "us_median": round(med * 1e3, 2),
-              "gbs": round(nb / med / 1e6, 1), "pct_peak": round(100 * nb / med / 1e6 / peak, 1)})
-    del qk, ds
+    # the benchmarked step, and a mid-size step (QK 4096 tokens + DSV4 2048
+    # tokens x 64 heads), with and without programmatic dependent launch
+    mid = (wl.make_qk(4096, 32, 8, 8, theta=1e6, max_pos=131072, seed=3, device=device),
+           wl.make_dsv4(2048, 64, max_pos=131072, num_blocks=64, block_size=64, seed=4,
+                        device=device))
+    for name, (qk, ds) in (("step", make_step_inputs(device)), ("step_mid", mid)):
+        nb = sum(step_bytes(qk, ds))
+        for pdl in (False, True):
+            old = kvq.set_programmatic_launch(pdl)
+            try:
+                def step():
+                    launch_qk(kvq, qk, stream)
+                    launch_dsv4(kvq, ds, stream)
+                step()
+                med, _ = _time_launch(step, 50, stream, flush if nb < 256 * 2**20 else None)
+            finally:
+                kvq.set_programmatic_launch(old)
+            emit({"sweep": name, "programmatic_launch": pdl, "bytes": nb,
+                  "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
+                  "pct_peak": round(100 * nb / med / 1e6 / peak, 1)})
+        del qk, ds
+    del mid
     # dispatch crossover between the small- and large-batch shapes
     for H in (64, 128):
         for T in (1, 4, 16, 64, 128, 256, 512, 1024, 4096):

@@ -308,17 +308,22 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
 uint32_t kvq_set_stage_wait_limit(uint32_t polls);
 
 /*
- * Programmatic dependent launch.  enable != 0: later launches of this library
- * carry CUDA's programmatic stream serialization attribute, so a kernel may be
- * scheduled while the kernel before it on the stream is still finishing.
- * Every kernel of this library first waits until the kernels it depends on
- * have completed and their writes are visible (griddepcontrol.wait), then
- * lets the next kernel be scheduled; results and stream order are those of
- * ordinary launches, and only the launch gaps shrink (short, launch-bound
- * calls such as decode steps, also inside CUDA graphs).  Default off.
- * Returns the previous setting (0 or 1).  Not synchronised with launches on
- * other threads.  No counterpart in the source pages: a launch option of this
- * library.
+ * Programmatic dependent launch.  enable != 0 (the default): launches of
+ * this library carry CUDA's programmatic stream serialization attribute, so a
+ * kernel may be scheduled while the kernel before it on the stream is still
+ * finishing.  Every kernel of this library first waits until the kernels it
+ * depends on have completed and their writes are visible
+ * (griddepcontrol.wait); its one-shot launch shapes then let the next kernel
+ * be scheduled (griddepcontrol.launch_dependents), its persistent shapes do
+ * not.  Results and stream order are those of ordinary launches; only the
+ * launch gaps shrink: on GB300 a 32-layer decode step captured in a CUDA
+ * graph goes from 2.47 to 1.79 us per launch, a mid-size step gains 3 %, and
+ * the 32768-token step is unchanged.  A kernel of the caller's that follows
+ * one of ours and was itself launched with the attribute must wait
+ * (griddepcontrol.wait or cudaGridDependencySynchronize) before reading our
+ * outputs, as with any programmatic launch.  Returns the previous setting
+ * (0 or 1).  Not synchronised with launches on other threads.  No
+ * counterpart in the source pages: a launch option of this library.
  */
 int kvq_set_programmatic_launch(int enable);
 

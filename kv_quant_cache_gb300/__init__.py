@@ -275,9 +275,9 @@ def set_stage_wait_limit(polls: int) -> int:
 
 
 def set_programmatic_launch(enable: bool) -> bool:
-    """Launch later kernels with programmatic stream serialization (they may be
-    scheduled while the previous kernel finishes; results are unchanged);
-    returns the previous setting."""
+    """Launch later kernels with programmatic stream serialization (the
+    default: they may be scheduled while the previous kernel finishes; results
+    are unchanged); returns the previous setting."""
     return bool(lib().kvq_set_programmatic_launch(1 if enable else 0))
 
 

@@ -102,7 +102,7 @@ namespace kvq {
 
 namespace {
 std::atomic<uint32_t> g_stage_wait_limit{1u << 22};
-std::atomic<bool> g_programmatic_launch{false};
+std::atomic<bool> g_programmatic_launch{true};
 }  // namespace
 
 bool programmatic_launch() { return g_programmatic_launch.load(std::memory_order_relaxed); }

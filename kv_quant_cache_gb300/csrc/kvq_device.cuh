@@ -48,12 +48,18 @@ __device__ __forceinline__ float group_max(float v) {
   return v;
 }
 
-// Programmatic dependent launch.  Every kernel starts with both: it waits
-// until the grids it depends on have completed and their writes are visible
-// (a no-op when it was launched the ordinary way), then lets the next grid on
-// the stream be scheduled while it runs.
-__device__ __forceinline__ void grid_dependency_sync() {
+// Programmatic dependent launch.  Every kernel starts by waiting until the
+// grids it depends on have completed and their writes are visible (a no-op
+// when it was launched the ordinary way).  One-shot grids then let the next
+// grid on the stream be scheduled: it can start once their last wave runs.
+// Persistent grids do not: all their CTAs are resident from the start, so a
+// dependent scheduled early would only sit on their SMs, waiting.
+__device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_sync() {
+  grid_dependency_wait();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 

@@ -308,7 +308,7 @@ __device__ __forceinline__ void stream_q(const Dsv4Params& p, int gw, int nw, in
 template <int WARPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_stream_kernel(const Dsv4Params p) {
-  grid_dependency_sync();
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int gw = (int)blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = (int)gridDim.x * WARPS;

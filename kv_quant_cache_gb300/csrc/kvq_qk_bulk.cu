@@ -136,7 +136,7 @@ __device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, i
 template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 qk_bulk_kernel(const BulkParams p) {
-  grid_dependency_sync();
+  grid_dependency_wait();
   constexpr int kCsAt = STAGE_BYTES;           // cos/sin row inside a stage
   constexpr int kStage = STAGE_BYTES + 4 * D;  // room for a full-width cos/sin row
   constexpr int LPR = D / (2 * kF);            // lanes per row

@@ -188,7 +188,7 @@ qk_tiles_kernel(const QkParams p) {
 template <int WARPS, int STEPS, int MINB>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 qk_stream_kernel(const QkParams p) {
-  grid_dependency_sync();
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;

@@ -274,10 +274,10 @@ def test_stage_wait_limit_round_trip(L):
 
 
 def test_programmatic_launch_switch(L):
-    old = kvq.set_programmatic_launch(True)
+    old = kvq.set_programmatic_launch(False)
     try:
-        assert old is False
-        assert kvq.set_programmatic_launch(False) is True
+        assert old is True   # on by default
         assert kvq.set_programmatic_launch(True) is False
+        assert kvq.set_programmatic_launch(False) is True
     finally:
         kvq.set_programmatic_launch(old)
