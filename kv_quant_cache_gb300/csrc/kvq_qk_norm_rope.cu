@@ -4,7 +4,7 @@
 // FusedQkNormRope"), section "Summary": Q and K heads of a packed
 // [T, (Hq+Hk+Hv)*D] bf16 tensor get per-head RMSNorm followed by NeoX RoPE in
 // place, V untouched, separate [D] weights, and the NeoX partner read with
-// its own dimension's weight.  This build covers the guarded case of "Notes
+// its own dimension's weight.  This file covers the guarded case of "Notes
 // for Reviewers": bf16, D = 128, full-dimension NeoX rotation.
 //
 // Mapping on sm_103a.  A 128-dim bf16 head row is 256 bytes; a half-warp
