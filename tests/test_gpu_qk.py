@@ -214,3 +214,44 @@ def test_general_staged_finishing_from_global_memory(cuda_device, layout):
             assert torch.equal(_run_layout(d, config), ref), kvq.configs("qk")[config]
     finally:
         kvq.set_stage_wait_limit(old)
+
+
+def test_staged_shape_at_131072_tokens(cuda_device):
+    """The largest QK workload of the sweep (131072 tokens, 5.2M head rows:
+    the staged shape's regime), every token against the oracle."""
+    d = wl.make_qk(131072, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001, device=cuda_device)
+    assert kvq.configs("qk")[kvq.qk_config_for(131072, 32, 8)].startswith("bulk")
+    rep = qk_parity(d, slice_tokens=16384)
+    assert rep.n == 131072 * 40 * 128
+
+
+def test_two_streams_at_once(cuda_device):
+    """Both operators enqueued on two streams at the same time (independent
+    buffers, programmatic launch on) give the bytes of a run on their own;
+    the QK result is also checked against the oracle."""
+    from gpu_cases import dsv4_parity, run_dsv4
+    qk = wl.make_qk(32768, 32, 8, 8, theta=1e6, max_pos=131072, seed=81, device=cuda_device)
+    ds = wl.make_dsv4(4096, 64, max_pos=131072, num_blocks=128, block_size=64, seed=82,
+                      device=cuda_device)
+    ref_qk = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in qk.items()}
+    ref_ds = {k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in ds.items()}
+    s1, s2 = torch.cuda.Stream(cuda_device), torch.cuda.Stream(cuda_device)
+    torch.cuda.synchronize()
+    for _ in range(3):  # same inputs each time: restore, then run both at once
+        qk["qkv"].copy_(ref_qk["qkv"])
+        ds["q"].copy_(ref_ds["q"])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            kvq.fused_qk_norm_rope(qk["qkv"], 32, 8, 8, 128, qk["eps"], qk["q_weight"],
+                                   qk["k_weight"], qk["cos_sin"], True, qk["positions"], stream=s1)
+        with torch.cuda.stream(s2):
+            kvq.dsv4_qnorm_rope_kv_rope_quant_insert(
+                ds["q"], ds["kv"], ds["eps"], ds["q_weight"], ds["kv_weight"], ds["cos_sin"],
+                ds["positions"], ds["slot_mapping"], ds["kv_cache"], stream=s2)
+        torch.cuda.synchronize()
+    got_qk, got_q, got_cache = qk["qkv"].clone(), ds["q"].clone(), ds["kv_cache"].clone()
+    qk_parity(ref_qk)            # reference: one operator at a time on the default stream
+    run_dsv4(ref_ds)
+    torch.cuda.synchronize()
+    assert torch.equal(got_qk, ref_qk["qkv"])
+    assert torch.equal(got_q, ref_ds["q"]) and torch.equal(got_cache, ref_ds["kv_cache"])
