@@ -35,6 +35,20 @@ def test_c_client_compiles_and_links(tmp_path):
     assert os.path.exists(_compile(str(tmp_path)))
 
 
+def test_header_is_valid_cpp(tmp_path):
+    """include/kvq.h also compiles as C++ (extern "C" linkage, no C-only
+    constructs)."""
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("g++ not available")
+    src = tmp_path / "use_header.cpp"
+    src.write_text('#include "kvq.h"\nint main() { return kvq_status_string(KVQ_OK) ? 0 : 1; }\n')
+    r = subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+
+
 @pytest.mark.gpu
 def test_c_client_runs(tmp_path, cuda_device):
     exe = _compile(str(tmp_path))
