@@ -609,6 +609,30 @@ def sweep(kvq, device):
               "gbs": round(mb * 2**20 / med / 1e6, 1),
               "pct_peak": round(100 * mb * 2**20 / med / 1e6 / peak, 1)})
         del src, dst
+    # the same crossover for two general layouts: one-shot general kernel vs
+    # the staged shape
+    gen = names.index("general<frag4>")
+    stg = names.index("bulk<16w,2st,6KB>")
+    for D, rot, neox in ((64, 64, True), (256, 64, False)):
+        for T in (1024, 4096, 8192, 16384, 32768):
+            d = wl.make_qk(T, 32, 8, 8, D=D, theta=1e6, max_pos=131072, seed=9 + T, device=device,
+                           rotary_dim=rot, is_neox=neox)
+            nb = qk_bytes(T, 32, 8, D, rot)
+            res = {}
+            for cid in (gen, stg):
+                old = kvq.set_config("qk", cid)
+                try:
+                    res[names[cid]] = round(_time_launch(
+                        lambda: kvq.fused_qk_norm_rope(d["qkv"], 32, 8, 8, D, d["eps"],
+                                                       d["q_weight"], d["k_weight"], d["cos_sin"],
+                                                       neox, d["positions"], stream=stream,
+                                                       rotary_dim=rot),
+                        30, stream, flush if nb < 256 * 2**20 else None)[0] * 1e3, 2)
+                finally:
+                    kvq.set_config("qk", old)
+            emit({"sweep": "qk_dispatch_general", "D": D, "rot": rot, "neox": neox, "T": T,
+                  "rows": T * 40, "bytes": nb, "us": res})
+            del d
     # a copy moving the QK step's bytes (Q+K rows read and written): the
     # ceiling for a launch of that length
     nb = qk_bytes(wl.QK_LARGE.T, wl.QK_LARGE.Hq, wl.QK_LARGE.Hk)

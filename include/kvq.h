@@ -277,7 +277,9 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * configuration computes bit-identical results.  QK configurations 0-4
  * (register-pipelined) and 7-9 (TMA-staged, bulk<...>) are launch shapes of
  * the head_dim-128 full-NeoX kernels and agree bit for bit; layouts other
- * than that one take the general kernel with 4-dim fragments.  QK
+ * than that one take the general kernel with 4-dim fragments below 2^19 Q+K
+ * rows per call and the staged shape from there on (kvq_qk_config_for
+ * describes the head_dim-128 full-NeoX layout).  QK
  * configurations 5 and 6 force the general kernel, with 4- or 8-dim
  * fragments, for every layout; its sum of squares is added in another order,
  * so it agrees with the others within the operator's rounding, not bit for

@@ -39,6 +39,10 @@ constexpr int kQkGeneralFrag = 4;
 // the one-shot general kernel by 2-10 % at 650K-1.3M rows.
 constexpr int64_t kQkSmallRows = 152 * 8;
 constexpr int64_t kQkStagedRows = (int64_t)1 << 20;
+// The other layouts' one-shot general kernel gives way to the staged shape
+// earlier (same sweeps: staged 3-13 % faster from 655K rows on at head_dim 64
+// and 256, within a few percent at 330K).
+constexpr int64_t kQkGeneralStagedRows = (int64_t)1 << 19;
 
 std::atomic<int64_t> g_threshold{-1};
 std::atomic<int> g_dsv4_config{-1};
@@ -168,8 +172,12 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   a.max_pos = max_pos;
   a.errors = reinterpret_cast<int*>(errors);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const bool small = num_tokens * (int64_t)rows < kQkSmallRows;
-  const int config = qk_config_for(num_tokens, rows);
+  const int64_t n = num_tokens * (int64_t)rows;
+  const bool small = n < kQkSmallRows;
+  const bool tuned = head_dim == 128 && is_neox == 1 && rotary_dim == 128;
+  int config = qk_config_for(num_tokens, rows);
+  if (!tuned && g_qk_config.load(std::memory_order_relaxed) < 0 && n >= kQkGeneralStagedRows)
+    config = kQkStagedConfig;
   if (config == kQkGeneralFrag4Config || config == kQkGeneralFrag8Config)
     return finish_launch(
         kvq::launch_qk_general(a, small, config == kQkGeneralFrag8Config ? 8 : 4, st));
@@ -177,8 +185,7 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   const int shape = config - kvq::kQkFirstBulk;
   if (errors == nullptr && shape >= 0 && kvq::qk_bulk_eligible(a, shape))
     return finish_launch(kvq::launch_qk_bulk(a, shape, st));
-  if (head_dim == 128 && is_neox == 1 && rotary_dim == 128)
-    return finish_launch(kvq::launch_qk_norm_rope(a, config, st));
+  if (tuned) return finish_launch(kvq::launch_qk_norm_rope(a, config, st));
   return finish_launch(kvq::launch_qk_general(a, small && shape < 0, kQkGeneralFrag, st));
 }
 
