@@ -32,6 +32,7 @@
 // direct global loads, which give the same bits.  A stalled copy costs time,
 // never correctness.
 #include <atomic>
+#include <cstring>
 
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
@@ -49,6 +50,7 @@ constexpr int kUnroll = 4;               // row steps computed together
 using namespace tma;
 
 struct BulkParams {
+  CUtensorMap rows_map;  // tiled launches: [T][Hq + Hk][D] view of the Q/K rows
   __nv_bfloat16* qkv;
   const __nv_bfloat16* q_weight;
   const __nv_bfloat16* k_weight;
@@ -133,9 +135,9 @@ __device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, i
   }
 }
 
-template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED>
 __global__ void __launch_bounds__(WARPS * 32, 1)
-qk_bulk_kernel(const BulkParams p) {
+qk_bulk_kernel(const __grid_constant__ BulkParams p) {
   grid_dependency_wait();
   constexpr int kCsAt = STAGE_BYTES;           // cos/sin row inside a stage
   constexpr int kStage = STAGE_BYTES + 4 * D;  // room for a full-width cos/sin row
@@ -188,10 +190,16 @@ qk_bulk_kernel(const BulkParams p) {
       const Item it = item_at(p, gw + k * nw);
       const uint32_t stage = ring_s + (uint32_t)(k % NS) * kStage;
       const uint32_t bar = bar0 + 8u * (k % NS);
-      const uint32_t bytes = (uint32_t)it.nr * (2u * D);
       fence_proxy_async();
-      mbar_arrive_expect_tx(bar, bytes + cs_bytes);
-      bulk_load(stage, global_row<D>(p, it, 0), bytes, bar, pol);
+      if (TILED) {
+        // The whole box arrives: rows past the token's Q/K rows read as zero.
+        mbar_arrive_expect_tx(bar, (uint32_t)p.chunk_rows * (2u * D) + cs_bytes);
+        tile_load_3d(stage, &p.rows_map, 0, it.r0, it.t, bar, pol);
+      } else {
+        const uint32_t bytes = (uint32_t)it.nr * (2u * D);
+        mbar_arrive_expect_tx(bar, bytes + cs_bytes);
+        bulk_load(stage, global_row<D>(p, it, 0), bytes, bar, pol);
+      }
       bulk_load(stage + kCsAt, p.cos_sin + pos * p.rot, cs_bytes, bar, pol);
     }
   };
@@ -236,15 +244,16 @@ void chunking(const QkArgs& a, int rmax, int* chunks, int* chunk_rows) {
   *chunk_rows = (rows + *chunks - 1) / *chunks;
 }
 
-template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED>
 cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   static_assert(smem_bytes<D, WARPS, NS, STAGE_BYTES>() <= 227 * 1024, "shared memory per CTA");
   static std::atomic<int> cache[kMaxDevices];
   int per_sm = 0;
-  cudaError_t e = prepare(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>, WARPS * 32,
+  cudaError_t e = prepare(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED>, WARPS * 32,
                           smem_bytes<D, WARPS, NS, STAGE_BYTES>(), cache, &per_sm);
   if (e != cudaSuccess) return e;
   BulkParams p;
+  memset(&p.rows_map, 0, sizeof p.rows_map);
   p.qkv = static_cast<__nv_bfloat16*>(a.qkv);
   p.q_weight = static_cast<const __nv_bfloat16*>(a.q_weight);
   p.k_weight = static_cast<const __nv_bfloat16*>(a.k_weight);
@@ -258,27 +267,35 @@ cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   p.items = a.num_tokens * p.chunks;
   p.eps = a.eps;
   p.wait_limit = stage_wait_limit();
+  if (TILED) {
+    // [T][Hq + Hk][D] view: a token's V rows lie outside it.
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_rows, (cuuint64_t)a.num_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.row_elems * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)p.chunk_rows, 1};
+    if (!encode_bf16_3d(&p.rows_map, p.qkv, dims, strides, box))
+      return launch_layout<D, NEOX, WARPS, NS, STAGE_BYTES, false>(a, stream);
+  }
   int64_t grid = (int64_t)per_sm * device_sm_count();
   const int64_t need = (p.items + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  return launch_kernel(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES>, dim3((unsigned)grid),
+  return launch_kernel(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED>, dim3((unsigned)grid),
                        dim3(WARPS * 32), smem_bytes<D, WARPS, NS, STAGE_BYTES>(), stream, p);
 }
 
-template <int WARPS, int NS, int STAGE_BYTES>
+template <int WARPS, int NS, int STAGE_BYTES, bool TILED>
 cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
   const bool neox = a.is_neox != 0;
   switch (a.head_dim) {
     case 64:
-      return neox ? launch_layout<64, true, WARPS, NS, STAGE_BYTES>(a, stream)
-                  : launch_layout<64, false, WARPS, NS, STAGE_BYTES>(a, stream);
+      return neox ? launch_layout<64, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<64, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
     case 128:
-      return neox ? launch_layout<128, true, WARPS, NS, STAGE_BYTES>(a, stream)
-                  : launch_layout<128, false, WARPS, NS, STAGE_BYTES>(a, stream);
+      return neox ? launch_layout<128, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<128, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
     case 256:
-      return neox ? launch_layout<256, true, WARPS, NS, STAGE_BYTES>(a, stream)
-                  : launch_layout<256, false, WARPS, NS, STAGE_BYTES>(a, stream);
+      return neox ? launch_layout<256, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<256, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -287,7 +304,7 @@ cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
 
 bool qk_bulk_eligible(const QkArgs& a, int shape) {
   static constexpr int kStageBytes[] = {
-#define KVQ_STAGE(W, S, KB) KB * 1024,
+#define KVQ_STAGE(W, S, KB, T) KB * 1024,
       KVQ_QK_BULK_SHAPES(KVQ_STAGE)
 #undef KVQ_STAGE
   };
@@ -302,7 +319,7 @@ bool qk_bulk_eligible(const QkArgs& a, int shape) {
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream) {
   using Launch = cudaError_t (*)(const QkArgs&, cudaStream_t);
   static constexpr Launch kLaunch[] = {
-#define KVQ_LAUNCH(W, S, KB) &launch_shape<W, S, KB * 1024>,
+#define KVQ_LAUNCH(W, S, KB, T) &launch_shape<W, S, KB * 1024, T != 0>,
       KVQ_QK_BULK_SHAPES(KVQ_LAUNCH)
 #undef KVQ_LAUNCH
   };

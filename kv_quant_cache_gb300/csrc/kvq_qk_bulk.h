@@ -10,11 +10,11 @@
 namespace kvq {
 
 // Staged launch shapes X(warps per CTA, stages per warp, KB of head rows per
-// stage), in the order of their QK configuration entries (named
-// bulk<Ww,Sst,KKB>).  A stage holds KB * 1024 / (2 head_dim) rows plus one
-// cos/sin row.
-#define KVQ_QK_BULK_SHAPES(X) X(16, 2, 6) X(24, 2, 3) X(24, 3, 2)
-#define KVQ_QK_BULK_COUNT(W, S, KB) +1
+// stage, tiled), in the order of their QK configuration entries (named
+// bulk<Ww,Sst,KKB> and, for tiled tensor-map copies, bulk<Ww,Sst,KKB,tile>).
+// A stage holds KB * 1024 / (2 head_dim) rows plus one cos/sin row.
+#define KVQ_QK_BULK_SHAPES(X) X(16, 2, 6, 0) X(24, 2, 3, 0) X(24, 3, 2, 0) X(16, 2, 6, 1)
+#define KVQ_QK_BULK_COUNT(W, S, KB, T) +1
 constexpr int kQkBulkShapes = 0 KVQ_QK_BULK_SHAPES(KVQ_QK_BULK_COUNT);
 // Index of the first staged shape in the QK configuration table.
 constexpr int kQkFirstBulk = 7;

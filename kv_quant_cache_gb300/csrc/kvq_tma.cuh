@@ -1,12 +1,14 @@
-// kvq_tma.cuh -- the bulk-copy (TMA) staging primitives shared by the staged
-// launch shapes of both operators: mbarrier set-up and bounded waits, 1-D
-// bulk copies global -> shared with an L2 evict-first policy, the proxy
-// fence, and the host-side helpers (pointer kind, per-device shared-memory
-// opt-in).  Inline PTX for sm_103a.
+// kvq_tma.cuh -- the bulk-copy (TMA) staging primitives of the staged launch
+// shapes: mbarrier set-up and bounded waits, 1-D bulk copies and tiled
+// tensor-map copies global -> shared with an L2 evict-first policy, the proxy
+// fence, and the host-side helpers (pointer kind, tensor-map encoding,
+// per-device shared-memory opt-in).  Inline PTX for sm_103a.
 #pragma once
 
 #include <atomic>
+#include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -101,6 +103,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Tiled copy of the box at (c0, c1, c2) of a 3-D tensor map -> shared,
+// completing on `bar`.  `tmap` is the map's address in parameter space
+// (a __grid_constant__ kernel parameter).
+__device__ __forceinline__ void tile_load_3d(uint32_t dst, const CUtensorMap* tmap, int c0,
+                                             int c1, int c2, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // Orders this thread's earlier shared-memory accesses before later
 // bulk-copy writes to the same stage.
 __device__ __forceinline__ void fence_proxy_async() {
@@ -117,6 +131,42 @@ inline bool device_memory(const void* ptr) {
     return false;
   }
   return attr.type == cudaMemoryTypeDevice;
+}
+
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime
+// (no link against the driver library); nullptr if unavailable.
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiled encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// A 3-D bf16 tensor map: dims[0] contiguous elements, strides (bytes) of
+// dims 1 and 2, box `box`; no swizzle (the box lands densely, row after row),
+// out-of-range elements read as zero.  False if it cannot be encoded.
+inline bool encode_bf16_3d(CUtensorMap* map, const void* base, const cuuint64_t dims[3],
+                           const cuuint64_t strides[2], const cuuint32_t box[3]) {
+  const EncodeTiled fn = encode_tiled();
+  if (fn == nullptr) return false;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Opts `kernel` in to `smem` bytes of dynamic shared memory and counts its
