@@ -275,7 +275,7 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * automatic dispatch picks one by problem size; the override forces one for
  * every later call of the process (benchmark sweeps, tests).  Every DSV4
  * configuration computes bit-identical results.  QK configurations 0-4
- * (register-pipelined) and 7-9 (TMA-staged, bulk<...>) are launch shapes of
+ * (register-pipelined) and 7-10 (TMA-staged, bulk<...>) are launch shapes of
  * the head_dim-128 full-NeoX kernels and agree bit for bit; layouts other
  * than that one take the general kernel with 4-dim fragments below 2^19 Q+K
  * rows per call and the staged shape from there on (kvq_qk_config_for
