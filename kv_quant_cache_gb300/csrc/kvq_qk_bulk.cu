@@ -14,7 +14,10 @@
 // (token, chunk of at most RMAX consecutive Q/K head rows, the chunks of a
 // token balanced in length); a stage holds STAGE_BYTES of rows, so RMAX =
 // STAGE_BYTES / (2 D).  The item's rows are one contiguous span of qkv and
-// arrive with one cp.async.bulk; the token's cos/sin row (4 rot bytes)
+// arrive with one cp.async.bulk (TILED: one cp.async.bulk.tensor box of a
+// [T][Hq+Hk][D] tensor map, rows past the token's Q/K rows read as zero and
+// never written -- measured slower, kept as a launch shape); the token's
+// cos/sin row (4 rot bytes)
 // arrives with a second; both complete on the stage's mbarrier, and both
 // carry an L2 evict-first policy (each byte is read once).  Lane 0 keeps NS
 // items in flight: when the warp has consumed a stage it issues the item NS
