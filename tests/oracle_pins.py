@@ -287,6 +287,35 @@ def pin_qk_rope_complex(L):
     np.testing.assert_allclose(lhs, rhs, rtol=1e-12)
 
 
+def pin_qk_rope_partial(L):
+    """Partial rotation at head_dim 64 and 256, NeoX and interleaved pairs
+    [IO1019 "Summary": the API carries is_neox; rotary_dim < head_dim rotates
+    the leading dims]: the first rotary_dim dims of each head equal complex
+    multiplication of their pairs by the table row (width rotary_dim), and
+    every dim from rotary_dim on keeps its unrotated normalised value."""
+    T, Hq, Hk, Hv = 3, 2, 1, 1
+    pos = np.array([1, 700, 2000], np.int64)
+    for D in (64, 256):
+        for rot in (16, D // 2):
+            for neox in (True, False):
+                d = wl.make_qk(T, Hq, Hk, Hv, D, 1e4, 4096, "uniform", 7 + D + rot,
+                               rotary_dim=rot)
+                base = dict(qkv=wl.bf16_bits(d["qkv"]), q_weight=wl.bf16_bits(d["q_weight"]),
+                            k_weight=wl.bf16_bits(d["k_weight"]), cos_sin=wl.host(d["cos_sin"]))
+
+                def run(positions):
+                    return oracle.qk_norm_rope(base["qkv"], Hq, Hk, Hv, D, EPS, base["q_weight"],
+                                               base["k_weight"], base["cos_sin"], positions,
+                                               is_neox=neox, rot_dim=rot, want_ref=True,
+                                               nthreads=1, _lib=L)
+                _, n0, _ = run(np.zeros(T, np.int64))          # position 0: no rotation
+                _, nr, mag = run(pos)
+                want = _complex_rotate(n0, base["cos_sin"][pos][:, None, :], neox, 0, rot)
+                assert np.all(np.abs(nr - want) <= 1e-14 * mag + 1e-300), (D, rot, neox)
+                assert np.array_equal(nr[..., rot:], n0[..., rot:]), (D, rot, neox)
+                assert not np.allclose(nr[..., :rot], n0[..., :rot])
+
+
 def pin_qk_partner_weight(L):
     D = 128
     rng = np.random.default_rng(4)
@@ -491,7 +520,7 @@ ALL_PINS = [
     pin_bf16_value_and_roundtrip, pin_bf16_vs_torch, pin_bf16_single_rounding,
     pin_e4m3_decode_vs_torch, pin_e4m3_roundtrip, pin_e4m3_vs_torch,
     pin_ue8m0_hand, pin_ue8m0_bruteforce,
-    pin_qk_textbook_rmsnorm, pin_qk_all_equal_row, pin_qk_rope_complex,
+    pin_qk_textbook_rmsnorm, pin_qk_all_equal_row, pin_qk_rope_complex, pin_qk_rope_partial,
     pin_qk_partner_weight, pin_qk_pairing_index, pin_qk_v_untouched,
     pin_dsv4_hand_entry, pin_dsv4_skip_and_addressing, pin_dsv4_q_textbook,
     pin_dsv4_kv_decisions, pin_slicing_and_threads, pin_gather_hand_entry, pin_gather_round_trip,

@@ -29,6 +29,12 @@ MUTANTS = {
     "neox_partner_index": ("int b = neox ? off + i + half", "int b = neox ? off + i + 1"),
     "interleaved_as_neox": ("int a = neox ? off + i : off + 2 * i;", "int a = off + i;"),
     "dsv4_rope_offset": ("DSV4_ROPE_OFF = 448,", "DSV4_ROPE_OFF = 384,"),
+    # partial rotation (positions in the pins stay far enough from the end of
+    # the table that the widened reads stay inside it)
+    "partial_rotates_whole_head": ("rope_rotate(n, mg, 0, A->rot, A->neox, cs);",
+                                   "rope_rotate(n, mg, 0, A->D, A->neox, cs);"),
+    "partial_table_stride": ("const float* cs = A->cs + pos * A->rot;",
+                             "const float* cs = A->cs + pos * (A->rot / 2);"),
     "qk_q_k_weights_swapped": ("h < A->Hq ? A->qw : A->kw", "h < A->Hk ? A->qw : A->kw"),
     "qk_v_not_copied": ("  if (out != in)\n    memcpy(", "  if (0)\n    memcpy("),
     # codecs
