@@ -288,7 +288,7 @@ def pin_qk_rope_complex(L):
 
 
 def pin_qk_rope_partial(L):
-    """Partial rotation at head_dim 64 and 256, NeoX and interleaved pairs
+    """Partial and full rotation at head_dim 64 and 256, NeoX and interleaved pairs
     [IO1019 "Summary": the API carries is_neox; rotary_dim < head_dim rotates
     the leading dims]: the first rotary_dim dims of each head equal complex
     multiplication of their pairs by the table row (width rotary_dim), and
@@ -296,7 +296,7 @@ def pin_qk_rope_partial(L):
     T, Hq, Hk, Hv = 3, 2, 1, 1
     pos = np.array([1, 700, 2000], np.int64)
     for D in (64, 256):
-        for rot in (16, D // 2):
+        for rot in (16, D // 2, D):
             for neox in (True, False):
                 d = wl.make_qk(T, Hq, Hk, Hv, D, 1e4, 4096, "uniform", 7 + D + rot,
                                rotary_dim=rot)
