@@ -127,7 +127,10 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
  *   for each rotated pair (a, b) with frequency index i:
  *     out_a = n_a * cos_i - n_b * sin_i,   out_b = n_b * cos_i + n_a * sin_i
  * so the partner enters with its own dimension's weight.  head_dim 128 with
- * full NeoX rotation runs a tuned kernel; the other layouts a general one.
+ * full NeoX rotation runs tuned register-pipelined kernels, the other
+ * layouts a general one; large batches of every layout take a kernel that
+ * stages rows through shared memory with the bulk-copy (TMA) engine (launch
+ * shapes below).  Every path gives the same bits.
  * Source: InfiniOps PR #1019, "Summary" (the API carries is_neox, following
  * vLLM's fused_qk_norm_rope) and "Notes for Reviewers" (the fast path the
  * page guards to: bf16, head_dim 128, full-dimension NeoX).
