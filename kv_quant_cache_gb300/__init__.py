@@ -123,6 +123,8 @@ def _check(status: int, fn: str) -> None:
 def _cuda(t: torch.Tensor, dtype, name: str) -> int:
     """Address of a CUDA tensor, or of a pinned host tensor (mapped into the
     device's address space at the same address under unified addressing)."""
+    if type(t) is torch.Tensor and t.is_cuda and t.dtype == dtype and t.is_contiguous():
+        return t.data_ptr()  # the common case, checked first (per-call cost)
     if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu"
                                                              and t.is_pinned())):
         raise ValueError(f"{name}: expected a CUDA tensor or a pinned host tensor")
@@ -133,8 +135,15 @@ def _cuda(t: torch.Tensor, dtype, name: str) -> int:
     return t.data_ptr()
 
 
+# torch's current raw stream handle without building a Stream object (a few
+# times cheaper per call); the public API is the fallback.
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device) -> int:
     if stream is None:
+        if _raw_current_stream is not None and device.type == "cuda":
+            return _raw_current_stream(device.index)
         stream = torch.cuda.current_stream(device if device.type == "cuda" else None)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 

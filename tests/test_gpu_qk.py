@@ -255,3 +255,13 @@ def test_two_streams_at_once(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(got_qk, ref_qk["qkv"])
     assert torch.equal(got_q, ref_ds["q"]) and torch.equal(got_cache, ref_ds["kv_cache"])
+
+
+def test_default_stream_is_torchs_current_stream(cuda_device):
+    """Calls without `stream` enqueue on torch's current stream, also inside a
+    `torch.cuda.stream` context (the binding reads the raw handle)."""
+    s = torch.cuda.Stream(cuda_device)
+    assert kvq._stream(None, cuda_device) == torch.cuda.current_stream(cuda_device).cuda_stream
+    with torch.cuda.stream(s):
+        assert kvq._stream(None, cuda_device) == s.cuda_stream
+        assert kvq._stream(None, cuda_device) == torch.cuda.current_stream(cuda_device).cuda_stream
