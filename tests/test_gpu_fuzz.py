@@ -12,7 +12,7 @@ from gpu_cases import dsv4_parity, qk_parity, with_config, with_threshold
 pytestmark = pytest.mark.gpu
 
 
-def _qk_cases(n=40, seed=2024):
+def _qk_cases(n=100, seed=2024):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
@@ -42,7 +42,7 @@ def test_qk_random(cuda_device, case):
         qk_parity(d)
 
 
-def _dsv4_cases(n=40, seed=2025):
+def _dsv4_cases(n=80, seed=2025):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
