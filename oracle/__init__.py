@@ -69,6 +69,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_ue8m0_exponent.argtypes = [ctypes.c_double]
     lib.orc_ue8m0_byte.restype = ctypes.c_uint8
     lib.orc_ue8m0_byte.argtypes = [ctypes.c_double]
+    lib.orc_exponent_margin.restype = ctypes.c_double
+    lib.orc_exponent_margin.argtypes = [ctypes.c_double]
     for name in ("orc_bf16_round_n", "orc_e4m3_encode_n", "orc_ue8m0_byte_n"):
         getattr(lib, name).restype = None
         getattr(lib, name).argtypes = [_P, _P, _I64]

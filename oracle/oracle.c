@@ -113,6 +113,18 @@ uint8_t orc_ue8m0_byte(double amax) {
   return (uint8_t)b;
 }
 
+/* Relative distance of amax to the nearer of the two boundaries 448 * 2^(e-1)
+ * < amax <= 448 * 2^e that bracket its exponent decision e; HUGE_VAL for
+ * amax = 0 (no boundary).  A computation of amax that is off by less than
+ * this relative amount reaches the same exponent. */
+double orc_exponent_margin(double amax) {
+  if (!(amax > 0.0)) return HUGE_VAL;
+  const int e = orc_ue8m0_exponent(amax);
+  const double up = ldexp(448.0, e) / amax - 1.0;        /* >= 0 */
+  const double dn = 1.0 - ldexp(448.0, e - 1) / amax;    /* > 0 */
+  return up < dn ? up : dn;
+}
+
 void orc_bf16_round_n(const double* v, uint16_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_round(v[i]);
 }
@@ -345,34 +357,21 @@ static int dsv4_token(const void* p, int64_t t, double* n) {
   if (A->kv_ref)
     for (int i = 0; i < DSV4_DIM; ++i) A->kv_ref[krow + i] = n[i];
 
-  /* Exponent and codes per block.  Blocks cover dims 0..447, which the
-   * rotation does not touch.  Decisions in fp32 (reading R5). */
+  /* Exponent and codes per block, decided on the unrounded normalised values
+   * (reading R5).  Blocks cover dims 0..447, which the rotation does not
+   * touch. */
   uint8_t entry[DSV4_ENTRY];
   for (int b = 0; b < DSV4_NBLOCK; ++b) {
-    float f[DSV4_BLOCK];
-    float amax32 = 0.0f;
-    double amax64 = 0.0;
-    for (int j = 0; j < DSV4_BLOCK; ++j) {
-      double v = n[b * DSV4_BLOCK + j];
-      f[j] = (float)v;
-      if (fabsf(f[j]) > amax32) amax32 = fabsf(f[j]);
-      if (fabs(v) > amax64) amax64 = fabs(v);
-    }
-    uint8_t byte = orc_ue8m0_byte((double)amax32);
-    int e = (int)byte - 127;
+    const double* blk = n + b * DSV4_BLOCK;
+    double amax = 0.0;
     for (int j = 0; j < DSV4_BLOCK; ++j)
-      entry[b * DSV4_BLOCK + j] = orc_e4m3_encode(ldexp((double)f[j], -e));
+      if (fabs(blk[j]) > amax) amax = fabs(blk[j]);
+    const uint8_t byte = orc_ue8m0_byte(amax);
+    const int e = (int)byte - 127;
+    for (int j = 0; j < DSV4_BLOCK; ++j)
+      entry[b * DSV4_BLOCK + j] = orc_e4m3_encode(ldexp(blk[j], -e));
     entry[DSV4_SCALE_AT + b] = byte;
-    if (A->margin) {
-      double m = HUGE_VAL;
-      if (amax64 > 0.0) {
-        int ed = orc_ue8m0_exponent((double)amax32);
-        double up = fabs(amax64 / ldexp(448.0, ed) - 1.0);
-        double dn = fabs(amax64 / ldexp(448.0, ed - 1) - 1.0);
-        m = up < dn ? up : dn;
-      }
-      A->margin[t * DSV4_NBLOCK + b] = m;
-    }
+    if (A->margin) A->margin[t * DSV4_NBLOCK + b] = orc_exponent_margin(amax);
   }
   for (int i = 0; i < DSV4_ROPE; ++i) {
     uint16_t bits = orc_bf16_round(n[DSV4_ROPE_OFF + i]);

@@ -35,9 +35,13 @@
  *   R4 UE8M0 exponent e = smallest integer with 448 * 2^e >= amax; stored byte
  *      clamp(e + 127, 0, 254); codes = e4m3fn round-to-nearest-even of
  *      n * 2^-e with e = byte - 127.
- *   R5 the exponent and code decisions are taken in fp32 (the precision the
- *      CUDA kernels compute in): n is evaluated in fp64 and rounded once to
- *      fp32 before amax and encoding.
+ *   R5 the exponent and code decisions are taken on the unrounded (fp64)
+ *      normalised value n itself: amax, the exponent and n * 2^-e are exact
+ *      functions of n and the codes are rounded once from n * 2^-e.  The
+ *      pages fix no precision for these decisions; an implementation that
+ *      computes n in fp32 can land on the other side of an exponent boundary
+ *      or an e4m3 rounding midpoint, which the comparison tolerates (margin
+ *      below) rather than the oracle copying that precision.
  *   R6 cache entry (584 bytes) at byte offset slot * 584 of a contiguous
  *      [num_blocks, block_size, 584] uint8 cache: [0,448) e4m3 codes,
  *      [448,576) 64 bf16 RoPE'd values (little endian), [576,583) the seven
@@ -73,6 +77,10 @@ uint8_t orc_e4m3_encode(double v);
 int orc_ue8m0_exponent(double amax);
 /* clamp(orc_ue8m0_exponent(amax) + 127, 0, 254). */
 uint8_t orc_ue8m0_byte(double amax);
+/* Relative distance (|amax - B| / amax) from amax to the nearer of the two
+ * boundaries B = 448 * 2^(e-1) and 448 * 2^e that bracket its exponent
+ * decision e; HUGE_VAL for amax <= 0. */
+double orc_exponent_margin(double amax);
 
 /* Element-wise array forms of the three encoders above (for the tests). */
 void orc_bf16_round_n(const double* v, uint16_t* out, int64_t n);
@@ -115,9 +123,8 @@ int orc_qk_norm_rope(const uint16_t* qkv_in, uint16_t* qkv_out, int64_t T,
  *   kv_cache   uint8 [num_blocks, block_size, 584], written in place
  *   q_ref, q_mag   optional fp64 [T, H, 512]
  *   kv_ref, kv_mag optional fp64 [T, 512] (n after RoPE, before any rounding)
- *   exp_margin     optional fp64 [T, 7]: relative distance of the fp64 block
- *                  amax to the nearer of the two power-of-two boundaries that
- *                  bracket its exponent decision
+ *   exp_margin     optional fp64 [T, 7]: orc_exponent_margin of each block's
+ *                  amax (HUGE_VAL for an all-zero block)
  * Returns 0 or a negative code (-1 null, -2 shape, -3 position out of range,
  * -4 slot out of range).
  */

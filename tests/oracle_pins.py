@@ -15,6 +15,9 @@ None of these re-types the oracle's own formulas.
 """
 from __future__ import annotations
 
+import bisect
+import functools
+import math
 from fractions import Fraction
 
 import numpy as np
@@ -102,6 +105,41 @@ def brute_ue8m0_exponent(amax: float) -> int:
     return hi
 
 
+@functools.lru_cache(maxsize=1)
+def _e4m3_positive_values():
+    """Exact values of the finite non-negative e4m3fn codes 0..126, decoded by
+    torch's float8_e4m3fn (increasing with the code)."""
+    codes = np.arange(127, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return [Fraction(float(v)) for v in vals]
+
+
+def brute_e4m3_code(v: float) -> int:
+    """The e4m3fn code nearest to the exact value ``v`` (|v| <= 448), ties to
+    the even code, sign kept: a search over the decoded code values in exact
+    rational arithmetic."""
+    tab = _e4m3_positive_values()
+    a = abs(Fraction(v))
+    assert a <= 448
+    i = bisect.bisect_left(tab, a)
+    cands = [c for c in (i - 1, i) if 0 <= c < len(tab)]
+    best = min(cands, key=lambda c: (abs(tab[c] - a), c & 1))
+    return (0x80 if math.copysign(1.0, v) < 0 else 0) | best
+
+
+def brute_exponent_margin(amax: float) -> float:
+    """|amax - B| / amax for the nearer of the boundaries B = 448 * 2^(e-1),
+    448 * 2^e around amax's exponent decision e, in exact arithmetic."""
+    if amax <= 0:
+        return math.inf
+    A = Fraction(amax)
+    e = brute_ue8m0_exponent(amax)
+    hi = Fraction(448) * Fraction(2) ** e
+    lo = hi / 2
+    assert lo < A <= hi
+    return float(min((hi - A) / A, (A - lo) / A))
+
+
 # ---------------------------------------------------------------------------
 # scalar codecs
 # ---------------------------------------------------------------------------
@@ -157,6 +195,13 @@ def pin_e4m3_roundtrip(L):
     vals = np.array([L.orc_e4m3_value(int(c)) for c in codes])
     vals[codes == 0x80] = -0.0
     assert np.array_equal(oracle.e4m3_encode(vals, _lib=L), codes)
+    # one rounding from fp64: 2^-40 above the midpoint of 1.125 and 1.25 rounds
+    # up, 2^-40 below it down; the exact midpoints tie to the even code
+    assert L.orc_e4m3_encode(1.1875 + 2.0**-40) == 0x3A
+    assert L.orc_e4m3_encode(1.1875 - 2.0**-40) == 0x39
+    assert L.orc_e4m3_encode(1.1875) == 0x3A and L.orc_e4m3_encode(1.0625) == 0x38
+    for v in (1.1875 + 2.0**-40, 1.1875 - 2.0**-40, -(1.0625 + 2.0**-41), 3.0 * 2.0**-10):
+        assert L.orc_e4m3_encode(v) == brute_e4m3_code(v), v
 
 
 def pin_e4m3_vs_torch(L):
@@ -448,23 +493,151 @@ def pin_dsv4_q_textbook(L):
 
 
 def pin_dsv4_kv_decisions(L):
+    """Exponents and codes are decided on the unrounded normalised values
+    (reading R5): the exponent is the smallest e with 448 * 2^e >= the block's
+    exact amax, and each code is the e4m3 value nearest to the exact n * 2^-e,
+    both found by exhaustive search in rational arithmetic."""
     T = 12
     inp = _dsv4_inputs(T, 1, num_blocks=4, block_size=4)
     r = _run_dsv4(L, inp)
     ent = r["cache"].reshape(-1, 584)[inp["slot_mapping"]]
-    f32 = r["kv_ref"][:, :448].astype(np.float32).reshape(T, 7, 64)
-    amax = np.abs(f32).max(-1)
+    n64 = r["kv_ref"][:, :448].reshape(T, 7, 64)
+    amax = np.abs(n64).max(-1)
     for t in range(T):
         for b in range(7):
             e = brute_ue8m0_exponent(float(amax[t, b]))
             byte = min(max(e + 127, 0), 254)
             assert ent[t, 576 + b] == byte
-            scaled = np.ldexp(f32[t, b], -(byte - 127)).astype(np.float32)
-            want = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-            assert np.array_equal(ent[t, 64 * b:64 * (b + 1)], want)
+            want = [brute_e4m3_code(math.ldexp(float(v), -(byte - 127))) for v in n64[t, b]]
+            assert np.array_equal(ent[t, 64 * b:64 * (b + 1)], np.array(want, np.uint8)), (t, b)
     rope = np.ascontiguousarray(ent[:, 448:576]).view(np.uint16)
     assert _is_nearest_bf16(rope, r["kv_ref"][:, 448:]).all()
     assert np.all(ent[:, 583] == 0)
+
+
+def pin_dsv4_decisions_single_rounding(L):
+    """Codes are rounded once, from the exact n * 2^-e (reading R5), not from
+    an fp32 copy of it.  kv = 1 everywhere and eps = 2^-30 make r = (1 +
+    2^-30)^-1/2, a hair below 1.  Block 0 has weights 1.75 (so e = -8) and
+    19 * 2^-12, whose scaled value 1.1875 r lies 2^-31 (relative) below the
+    midpoint of codes 0x39 (1.125) and 0x3a (1.25): rounding once gives 0x39;
+    rounding to fp32 first lands on the midpoint and ties to the even 0x3a."""
+    w = np.ones(512)
+    w[0] = 1.75
+    w[1] = 19 * 2.0**-12
+    ones = _to_bits(np.ones(512))
+    cache = np.full((1, 1, 584), wl.SENTINEL, np.uint8)
+    res = oracle.dsv4(np.ascontiguousarray(ones.reshape(1, 1, 512)),
+                      np.ascontiguousarray(ones.reshape(1, 512)), 2.0**-30, ones, _to_bits(w),
+                      wl.host(wl.cos_sin_table(1, 64, 1e4)), np.zeros(1, np.int64),
+                      np.zeros(1, np.int64), cache, want_ref=True, _lib=L)
+    ent = cache.reshape(-1)
+    v = math.ldexp(float(res["kv_ref"][0, 1]), 8)
+    assert brute_e4m3_code(v) == 0x39 and brute_e4m3_code(float(np.float32(v))) == 0x3A
+    assert ent[576] == 119 and ent[0] == 0x7E
+    assert ent[1] == 0x39
+    # The exponent too is decided on the exact amax: with x_0 = 1 - 2^-8 and
+    # eps = 511 * 2^-25 - 2^-40 (both exact in bf16 / fp32), mean(x^2) + eps =
+    # 1 - 2^-40, so r exceeds 1 by about 2^-41 and block 1's amax 1.75 r lies
+    # just above 448 * 2^-8: e = -7 (byte 120).  Its fp32 copy is 1.75 (e = -8).
+    x = np.ones(512)
+    x[0] = 1 - 2.0**-8
+    w = np.ones(512)
+    w[64] = 1.75
+    eps = 511 * 2.0**-25 - 2.0**-40
+    assert float(np.float32(eps)) == eps
+    cache = np.full((1, 1, 584), wl.SENTINEL, np.uint8)
+    res = oracle.dsv4(np.ascontiguousarray(ones.reshape(1, 1, 512)),
+                      np.ascontiguousarray(_to_bits(x).reshape(1, 512)), eps, ones, _to_bits(w),
+                      wl.host(wl.cos_sin_table(1, 64, 1e4)), np.zeros(1, np.int64),
+                      np.zeros(1, np.int64), cache, want_ref=True, _lib=L)
+    amax = float(np.abs(res["kv_ref"][0, 64:128]).max())
+    assert amax > 1.75 and float(np.float32(amax)) == 1.75
+    assert brute_ue8m0_exponent(amax) == -7
+    assert cache.reshape(-1)[577] == 120
+
+
+def pin_dsv4_exp_margin(L):
+    """The exponent margin the comparison relies on: for every block, the
+    relative distance of the exact amax to the nearer boundary 448 * 2^k that
+    brackets its exponent, in rational arithmetic; hand values at and near
+    boundaries; an all-zero block has no boundary."""
+    T = 10
+    inp = _dsv4_inputs(T, 1, num_blocks=4, block_size=4)
+    inp["kv"][3, :64] = 0                      # token 3, block 0: all zero
+    r = _run_dsv4(L, inp)
+    amax = np.abs(r["kv_ref"][:, :448].reshape(T, 7, 64)).max(-1)
+    want = np.array([[brute_exponent_margin(float(a)) for a in row] for row in amax])
+    got = r["exp_margin"]
+    assert np.isinf(got[3, 0]) and np.isinf(want[3, 0])
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isfinite(got), fin)
+    np.testing.assert_allclose(got[fin], want[fin], rtol=1e-12, atol=0)
+    assert L.orc_exponent_margin(448.0) == 0.0
+    assert L.orc_exponent_margin(3.5) == 0.0
+    m = L.orc_exponent_margin(3.5 * (1 + 2.0**-10))     # just above 448 * 2^-7
+    assert abs(m - 2.0**-10 / (1 + 2.0**-10)) <= 1e-15
+    m = L.orc_exponent_margin(448.0 * 0.75)             # midway (in ratio) of [224, 448]
+    assert abs(m - 1.0 / 3.0) <= 1e-15
+    assert math.isinf(L.orc_exponent_margin(0.0))
+
+
+def _term_magnitudes(n0, cs_rows, neox, off, rot):
+    """Sum of the magnitudes of the terms forming each rotated output, from
+    the unrotated values n0: with za = |x| + i|y| (the pair) and wa = |c| +
+    i|s| (the table row), the first element's terms sum to Re(za conj(wa)) and
+    the second's to Im(za wa); dims outside the rotation keep |n0|."""
+    half = rot // 2
+    c = np.abs(cs_rows[..., :half].astype(np.float64))
+    s = np.abs(cs_rows[..., half:rot].astype(np.float64))
+    part = np.abs(n0[..., off:off + rot])
+    za = (part[..., :half] + 1j * part[..., half:]) if neox else \
+        (part[..., 0::2] + 1j * part[..., 1::2])
+    wa = c + 1j * s
+    first, second = (za * np.conj(wa)).real, (za * wa).imag
+    out = np.abs(n0).copy()
+    if neox:
+        out[..., off:off + half], out[..., off + half:off + rot] = first, second
+    else:
+        out[..., off:off + rot:2], out[..., off + 1:off + rot:2] = first, second
+    return out
+
+
+def pin_qk_mag(L):
+    """The magnitude sums the comparison's cancellation term uses, for full
+    and partial rotation, both pairings, against the textbook RMSNorm
+    (torch) and a complex-number form of the rotation's terms."""
+    T, Hq, Hk, Hv = 3, 2, 1, 1
+    pos = np.array([0, 9, 3000], np.int64)
+    for D, rot, neox in ((128, 128, True), (64, 32, False), (256, 64, True)):
+        d = wl.make_qk(T, Hq, Hk, Hv, D, 1e4, 4096, "uniform", 50 + D + rot, rotary_dim=rot)
+        qkv, qw, kw = wl.bf16_bits(d["qkv"]), wl.bf16_bits(d["q_weight"]), wl.bf16_bits(d["k_weight"])
+        cs = wl.host(d["cos_sin"])
+        _, ref, mag = oracle.qk_norm_rope(qkv, Hq, Hk, Hv, D, EPS, qw, kw, cs, pos, is_neox=neox,
+                                          rot_dim=rot, want_ref=True, nthreads=1, _lib=L)
+        x = qkv.reshape(T, Hq + Hk + Hv, D)
+        n0 = np.concatenate([
+            _textbook(x[:, :Hq].copy(), qw, D, EPS).reshape(T, Hq, D),
+            _textbook(x[:, Hq:Hq + Hk].copy(), kw, D, EPS).reshape(T, Hk, D)], axis=1)
+        want = _term_magnitudes(n0, cs[pos][:, None, :], neox, 0, rot)
+        np.testing.assert_allclose(mag, want, rtol=1e-12, atol=1e-300)
+        assert np.all(np.abs(ref) <= mag * (1 + 1e-12))
+        np.testing.assert_allclose(mag[0], np.abs(n0[0]), rtol=1e-12)   # position 0
+
+
+def pin_dsv4_mag(L):
+    """The same magnitude sums for the DSV4 q rows and kv vector (interleaved
+    rotation of dims 448..511)."""
+    T, H = 4, 2
+    inp = _dsv4_inputs(T, H)
+    r = _run_dsv4(L, inp)
+    cs = inp["cos_sin"][inp["positions"]]
+    n0q = _textbook(inp["q"].reshape(-1, 512), inp["q_weight"], 512).reshape(T, H, 512)
+    np.testing.assert_allclose(r["q_mag"], _term_magnitudes(n0q, cs[:, None, :], False, 448, 64),
+                               rtol=1e-12, atol=1e-300)
+    n0k = _textbook(inp["kv"], inp["kv_weight"], 512)
+    np.testing.assert_allclose(r["kv_mag"], _term_magnitudes(n0k, cs, False, 448, 64),
+                               rtol=1e-12, atol=1e-300)
 
 
 def pin_slicing_and_threads(L):
@@ -498,7 +671,7 @@ def pin_gather_hand_entry(L):
 
 def pin_gather_round_trip(L):
     """Insert then read back: each dequantised value is within half an e4m3
-    step of the fp32 value the codes were taken from (2^-4 relative for
+    step of the exact value the codes were taken from (2^-4 relative for
     normal codes, 2^(e-10) absolute below), and the rotary dims come back as
     the nearest bf16 of the exact values."""
     T = 16
@@ -508,7 +681,7 @@ def pin_gather_round_trip(L):
     got = _bf16_value(out)
     ent = r["cache"].reshape(-1, 584)[inp["slot_mapping"]]
     e = ent[:, 576:583].astype(np.int64) - 127
-    f32 = r["kv_ref"][:, :448].astype(np.float32).astype(np.float64).reshape(T, 7, 64)
+    f32 = r["kv_ref"][:, :448].reshape(T, 7, 64)
     scale = np.ldexp(1.0, e)[:, :, None]
     err = np.abs(got[:, :448].reshape(T, 7, 64) - f32)
     bound = np.maximum(np.abs(f32) * 2.0 ** -4, scale * 2.0 ** -10)
@@ -523,5 +696,7 @@ ALL_PINS = [
     pin_qk_textbook_rmsnorm, pin_qk_all_equal_row, pin_qk_rope_complex, pin_qk_rope_partial,
     pin_qk_partner_weight, pin_qk_pairing_index, pin_qk_v_untouched,
     pin_dsv4_hand_entry, pin_dsv4_skip_and_addressing, pin_dsv4_q_textbook,
-    pin_dsv4_kv_decisions, pin_slicing_and_threads, pin_gather_hand_entry, pin_gather_round_trip,
+    pin_dsv4_kv_decisions, pin_dsv4_decisions_single_rounding, pin_dsv4_exp_margin, pin_qk_mag,
+    pin_dsv4_mag,
+    pin_slicing_and_threads, pin_gather_hand_entry, pin_gather_round_trip,
 ]

@@ -1,21 +1,28 @@
 """Comparison of the CUDA path's outputs with the oracle's (test-side only).
 
 Tolerances (derived in the design notes):
-  * bf16 outputs: |gpu - exact| <= ulp_bf16(exact) + 2^-15 * mag, where exact
-    is the oracle's unrounded fp64 result and mag the sum of the magnitudes of
-    the terms that form it.  Away from cancellation the second term is 256x
-    smaller than the first, so this is "within one bf16 ulp"; where a RoPE
-    difference cancels to near zero it bounds the fp32 error of the terms
-    (a 512-term sum of squares and two products stay below (D + 8) 2^-24 <=
-    2^-15 relative).
+  * bf16 outputs: within one bf16 ulp of the oracle's unrounded fp64 result
+    ``exact``.  The one allowance beyond that is for results that cancel:
+    a value whose terms' magnitudes sum to ``mag`` (|n| for an unrotated
+    element, |n_a c| + |n_b s| for a rotated one) may differ from ``exact`` by
+    up to ulp + 2^-15 mag, but only where it cancels by at least
+    CANCEL_BITS bits (|exact| < 2^-CANCEL_BITS mag).  2^-15 bounds the
+    relative fp32 error of the terms (a 512-term sum of squares, a reciprocal
+    square root, two products and a fused multiply-add: below (D + 8) 2^-24);
+    such an error can reach a full ulp of the result only where the result is
+    that much smaller than its terms.  Every value that needs the allowance is
+    counted (``beyond_ulp``) and reported with the shallowest cancellation
+    among them.
   * UE8M0 exponent bytes, slot placement, untouched bytes, pad: bit-exact;
-    the only excused exponent mismatches are blocks whose fp64 amax lies
-    within 2^-20 (relative) of a power-of-two boundary, and they are counted.
+    the only excused exponent mismatches are blocks whose exact amax lies
+    within 2^-20 (relative) of a power-of-two boundary, and they are counted
+    (the tests assert none occur at their seeds).
   * e4m3 codes: >= 99.99 % bit-exact, the rest at most one code apart
     (codes compared in value order, +0 and -0 equal).
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -23,6 +30,7 @@ import numpy as np
 EXP_TIE_MARGIN = 2.0 ** -20
 CODE_EXACT_MIN = 0.9999
 MAG_TERM = 2.0 ** -15
+CANCEL_BITS = 6
 
 
 def bf16_values(bits: np.ndarray) -> np.ndarray:
@@ -33,7 +41,7 @@ def bf16_values(bits: np.ndarray) -> np.ndarray:
 def ulp_bf16(x: np.ndarray) -> np.ndarray:
     """Spacing of bf16 numbers at |x| (2^-133 below the normal range)."""
     _, e = np.frexp(np.abs(x))          # |x| in [2^(e-1), 2^e)
-    return np.ldexp(1.0, np.maximum(e - 8, -133))
+    return np.where(x == 0, 2.0 ** -133, np.ldexp(1.0, np.maximum(e - 8, -133)))
 
 
 @dataclass
@@ -41,7 +49,9 @@ class Bf16Report:
     n: int = 0
     exact: int = 0
     bad: int = 0
-    max_ulps: float = 0.0
+    beyond_ulp: int = 0            # within tolerance only through the cancellation allowance
+    min_cancel_bits: float = math.inf  # shallowest cancellation among those (log2 mag/|exact|)
+    max_ulps: float = 0.0          # largest |gpu - exact| in ulps of exact
     first_bad: list = field(default_factory=list)
 
     def add(self, gpu_bits, oracle_bits, ref, mag):
@@ -56,9 +66,16 @@ class Bf16Report:
         m = mag.ravel()[diff]
         err = np.abs(bf16_values(g[diff]) - r)
         ulp = ulp_bf16(r)
-        allowed = ulp + MAG_TERM * m
-        badm = ~(err <= allowed)
+        within = err <= ulp
+        cancels = np.abs(r) < 2.0 ** -CANCEL_BITS * m
+        excused = ~within & cancels & (err <= ulp + MAG_TERM * m)
+        badm = ~(within | excused)
         self.max_ulps = max(self.max_ulps, float(np.max(err / ulp)))
+        if excused.any():
+            self.beyond_ulp += int(excused.sum())
+            with np.errstate(divide="ignore"):
+                depth = np.log2(m[excused] / np.abs(r[excused]))
+            self.min_cancel_bits = min(self.min_cancel_bits, float(np.min(depth)))
         if badm.any():
             self.bad += int(badm.sum())
             for i in np.nonzero(badm)[0][:5]:
@@ -71,6 +88,13 @@ class Bf16Report:
     @property
     def exact_frac(self):
         return self.exact / max(self.n, 1)
+
+    def summary(self) -> str:
+        s = (f"{self.n} bf16 values: {self.exact_frac:.6f} equal to the oracle's rounding, "
+             f"max {self.max_ulps:.3f} ulp, {self.beyond_ulp} beyond 1 ulp")
+        if self.beyond_ulp:
+            s += f" (each a cancellation of >= {self.min_cancel_bits:.1f} bits)"
+        return s
 
 
 def code_order(c: np.ndarray) -> np.ndarray:
@@ -87,6 +111,12 @@ class CacheReport:
     exp_mismatch_ties: int = 0
     exp_mismatch_bad: int = 0
     rope: Bf16Report = field(default_factory=Bf16Report)
+
+    def summary(self) -> str:
+        frac = self.codes_exact / self.codes if self.codes else 1.0
+        return (f"{self.entries} entries: e4m3 codes {frac:.7f} exact "
+                f"({self.codes - self.codes_exact} one code apart), exponent near-ties "
+                f"{self.exp_mismatch_ties}; rotary part: {self.rope.summary()}")
 
     def check(self, what=""):
         assert self.exp_mismatch_bad == 0, f"{what}: {self.exp_mismatch_bad} exponent bytes differ"

@@ -12,7 +12,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("threshold", [None, SMALL_PATH, TILED_PATH], ids=["auto", "small", "tiled"])
-def test_decode_size_16_tokens(cuda_device, threshold):
+def test_decode_size_16_tokens(cuda_device, threshold, parity_log):
+    """The 16-token decode workload (64 heads, two tokens without a slot)."""
     d = wl.make_dsv4_workload(wl.DSV4_DECODE, device=cuda_device)
     assert int((d["slot_mapping"] < 0).sum()) == 2
     if threshold is None:
@@ -22,9 +23,10 @@ def test_decode_size_16_tokens(cuda_device, threshold):
             qrep, crep = dsv4_parity(d)
     assert crep.entries == 14
     assert crep.exp_mismatch_ties == 0
+    parity_log(qrep, crep)
 
 
-def test_prefill_32768x64_every_token(cuda_device):
+def test_prefill_32768x64_every_token(cuda_device, parity_log):
     """The benchmarked workload (default dispatch = the persistent launch),
     every token and the whole cache compared."""
     d = wl.make_dsv4_workload(wl.DSV4_LARGE, device=cuda_device)
@@ -32,20 +34,25 @@ def test_prefill_32768x64_every_token(cuda_device):
     qrep, crep = dsv4_parity(d, slice_tokens=1024)
     assert qrep.n == 32768 * 64 * 512
     assert crep.entries == 32768
-    print(f"q exact {qrep.exact_frac:.5f}; codes exact {crep.codes_exact / crep.codes:.7f}; "
-          f"exponent near-ties {crep.exp_mismatch_ties}")
+    assert crep.exp_mismatch_ties == 0
+    parity_log(qrep, crep)
 
 
 @pytest.mark.parametrize("w", [w for w in wl.DSV4_SWEEP if w.T <= 8192], ids=lambda w: w.name)
-def test_sweep_every_token(cuda_device, w):
-    dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), slice_tokens=512)
+def test_sweep_every_token(cuda_device, w, parity_log):
+    qrep, crep = dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), slice_tokens=512)
+    assert crep.exp_mismatch_ties == 0
+    parity_log(qrep, crep)
 
 
 @pytest.mark.parametrize("w", [w for w in wl.DSV4_SWEEP if w.T > 8192], ids=lambda w: w.name)
-def test_sweep_full_size_sampled(cuda_device, w):
+def test_sweep_full_size_sampled(cuda_device, w, parity_log):
     """Full-size launch; 1024 sampled tokens (plus the first and last 8) compared
     with the oracle, and the whole cache checked for untouched slots."""
-    dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), sample=1024, seed=w.seed)
+    qrep, crep = dsv4_parity(wl.make_dsv4_workload(w, device=cuda_device), sample=1024,
+                             seed=w.seed)
+    assert crep.exp_mismatch_ties == 0
+    parity_log(qrep, crep)
 
 
 @pytest.mark.parametrize("T", [1, 4, 17, 511, 512, 777, 1000])

@@ -49,8 +49,23 @@ MUTANTS = {
     "scale_offset": ("DSV4_SCALE_AT = 576", "DSV4_SCALE_AT = 575"),
     "rope_bytes_big_endian": ("entry[DSV4_ROPE_AT + 2 * i] = (uint8_t)(bits & 0xff);",
                               "entry[DSV4_ROPE_AT + 2 * i] = (uint8_t)(bits >> 8);"),
-    "amax_wrong_block": ("double v = n[b * DSV4_BLOCK + j];", "double v = n[b * DSV4_BLOCK + j + 1];"),
-    "codes_unscaled": ("orc_e4m3_encode(ldexp((double)f[j], -e))", "orc_e4m3_encode((double)f[j])"),
+    "amax_wrong_block": ("if (fabs(blk[j]) > amax) amax = fabs(blk[j]);",
+                         "if (fabs(blk[j + 1]) > amax) amax = fabs(blk[j + 1]);"),
+    "codes_unscaled": ("orc_e4m3_encode(ldexp(blk[j], -e))", "orc_e4m3_encode(blk[j])"),
+    "codes_rounded_via_fp32": ("orc_e4m3_encode(ldexp(blk[j], -e))",
+                               "orc_e4m3_encode((double)(float)ldexp(blk[j], -e))"),
+    "amax_rounded_to_fp32": ("const uint8_t byte = orc_ue8m0_byte(amax);",
+                             "const uint8_t byte = orc_ue8m0_byte((double)(float)amax);"),
+    # the comparison's excusal inputs: magnitude sums and exponent margins
+    "mag_ignores_table": ("mag[a] = fabs(na * c) + fabs(nb * s);", "mag[a] = fabs(na) + fabs(nb);"),
+    "mag_partner_swapped": ("mag[b] = fabs(nb * c) + fabs(na * s);",
+                            "mag[b] = fabs(na * c) + fabs(nb * s);"),
+    "mag_unrotated_dims": ("      for (int i = 0; i < D; ++i) mg[i] = fabs(n[i]);",
+                           "      for (int i = 0; i < D; ++i) mg[i] = 2.0 * fabs(n[i]);"),
+    "margin_zero": ("  return up < dn ? up : dn;", "  return 0.0;"),
+    "margin_one_side": ("  return up < dn ? up : dn;", "  return up;"),
+    "margin_wrong_boundary": ("const double dn = 1.0 - ldexp(448.0, e - 1) / amax;",
+                              "const double dn = 1.0 - ldexp(448.0, e - 2) / amax;"),
     # (kept inside the cache: a mutant must not write out of bounds)
     "slot_hardcoded_block": ("(blk * A->block_size + off)", "((blk * 64 + off) % A->num_slots)"),
     "skip_ignored": ("const int64_t s = A->slot[t];", "const int64_t s = A->slot[t] < 0 ? 0 : A->slot[t];"),
