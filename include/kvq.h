@@ -55,9 +55,13 @@
  *   - Arguments are validated on the host before anything is launched.  On
  *     any error status nothing was launched and no memory was touched.
  *   - num_tokens == 0 returns KVQ_OK without a launch (pointers may be NULL).
- *   - After the launch the CUDA launch error (if any) is fetched and cleared
- *     with cudaGetLastError and reported as KVQ_ERR_CUDA; the raw code is
- *     available from kvq_last_cuda_error().
+ *   - A launch that fails is reported as KVQ_ERR_CUDA (its error is taken
+ *     off the CUDA runtime's last-error state); the raw code is available
+ *     from kvq_last_cuda_error().  A successful call leaves that state
+ *     alone: an error still pending from earlier, unrelated work stays
+ *     pending for its owner.  (The library carries its own copy of the CUDA
+ *     runtime, linked statically, so its last-error state is not the
+ *     caller's in any case.)
  *   - Not checked by the plain entry points (no sizes cross them; the caller
  *     guarantees): 0 <= positions[t] < rows of cos_sin_cache; slot_mapping[t]
  *     == -1 or a slot inside the cache.  Violations are undefined behaviour;
@@ -311,6 +315,29 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * register-pipelined large-batch shape.
  */
 uint32_t kvq_set_stage_wait_limit(uint32_t polls);
+
+/*
+ * Staging events of the staged launch shapes on the current device, counted
+ * by the kernels in a status word of the library (one per device) since the
+ * last reset:
+ *   *fallbacks       warps that stopped staging because a stage wait ran out
+ *                    (or the limit above is 0) and finished from global
+ *                    memory -- results unchanged;
+ *   *drain_timeouts  of those, warps whose copies in flight still had not
+ *                    landed after the drain wait (2^22 polls or 100 ms per
+ *                    copy).  Such a warp still writes correct rows, but its
+ *                    CTA may exit while a bulk copy is writing into its
+ *                    shared memory, which the hardware leaves undefined; a
+ *                    non-zero count means results of work that ran on the
+ *                    device at the same time should not be trusted.
+ * reset != 0 zeroes both counters after reading them.  The call first waits
+ * for all work on the current device to finish (cudaDeviceSynchronize), so
+ * it is a diagnostic, not for the launch path.  NULL pointers:
+ * KVQ_ERR_NULL; a CUDA error (including one left by earlier asynchronous
+ * work): KVQ_ERR_CUDA.  No counterpart in the source pages: a health check
+ * of this library's bulk-copy staging.
+ */
+kvq_status kvq_stage_events(uint64_t* fallbacks, uint64_t* drain_timeouts, int reset);
 
 /*
  * Programmatic dependent launch.  enable != 0 (the default): launches of

@@ -87,6 +87,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.kvq_qk_config_for.argtypes = [_I64, _I, _I]
     L.kvq_set_stage_wait_limit.restype = ctypes.c_uint32
     L.kvq_set_stage_wait_limit.argtypes = [ctypes.c_uint32]
+    L.kvq_stage_events.restype = _I
+    L.kvq_stage_events.argtypes = [_P, _P, _I]
     L.kvq_set_programmatic_launch.restype = _I
     L.kvq_set_programmatic_launch.argtypes = [_I]
     L.kvq_dsv4_config_for.restype = _I
@@ -141,11 +143,46 @@ _raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream, device) -> int:
+    """Raw handle of ``stream`` (default: torch's current stream of ``device``,
+    a CUDA device index; -1 = the current device)."""
     if stream is None:
-        if _raw_current_stream is not None and device.type == "cuda":
-            return _raw_current_stream(device.index)
-        stream = torch.cuda.current_stream(device if device.type == "cuda" else None)
-    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        if _raw_current_stream is not None and device >= 0:
+            return _raw_current_stream(device)
+        stream = torch.cuda.current_stream(device if device >= 0 else None)
+    if hasattr(stream, "cuda_stream"):
+        sd = getattr(stream, "device", None)
+        if device >= 0 and sd is not None and sd.index is not None and sd.index != device:
+            raise ValueError(f"stream is on cuda:{sd.index}, the tensors on cuda:{device}")
+        return stream.cuda_stream
+    return int(stream)
+
+
+_current_device = torch.cuda.current_device
+
+
+def _device(*tensors) -> int:
+    """The one CUDA device that every CUDA tensor of a call is on (pinned host
+    tensors may take part on any device); -1 if none is a CUDA tensor."""
+    dev = -1
+    for t in tensors:
+        if t is not None and t.is_cuda:
+            d = t.get_device()
+            if dev < 0:
+                dev = d
+            elif d != dev:
+                raise ValueError(f"tensors on cuda:{dev} and cuda:{d}: every CUDA tensor of "
+                                 "one call must be on the same device")
+    return dev
+
+
+def _on(dev, fn, *args):
+    """Call the C entry point ``fn`` with ``dev`` as the current device: the
+    library launches on, and keeps its per-device set-up for, the current
+    device, so a call whose tensors live on another GPU switches to it."""
+    if dev >= 0 and dev != _current_device():
+        with torch.cuda.device(dev):
+            return fn(*args)
+    return fn(*args)
 
 
 def _counter(errors, name="errors"):
@@ -173,16 +210,17 @@ def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps
     if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rotary_dim:
         raise ValueError("cos_sin_cache must be [max_pos, rotary_dim]")
     T = qkv.shape[0]
+    dev = _device(qkv, q_weight, k_weight, cos_sin_cache, positions, errors)
     args = (_cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
             head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
             _cuda(k_weight, torch.bfloat16, "k_weight"),
             _cuda(cos_sin_cache, torch.float32, "cos_sin_cache"))
     tail = (int(rotary_dim), int(bool(is_neox)), _cuda(positions, torch.int64, "positions"))
     if errors is None:
-        st = lib().fused_qk_norm_rope_ex(*args, *tail, _stream(stream, qkv.device))
+        st = _on(dev, lib().fused_qk_norm_rope_ex, *args, *tail, _stream(stream, dev))
     else:
-        st = lib().fused_qk_norm_rope_checked(*args, cos_sin_cache.shape[0], *tail,
-                                              _counter(errors), _stream(stream, qkv.device))
+        st = _on(dev, lib().fused_qk_norm_rope_checked, *args, cos_sin_cache.shape[0], *tail,
+                 _counter(errors), _stream(stream, dev))
     _check(st, "fused_qk_norm_rope")
 
 
@@ -206,6 +244,8 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
         q_out = q
     if q_out.shape != q.shape:
         raise ValueError("q_out must have q's shape")
+    dev = _device(q, q_out, kv, q_weight, kv_weight, cos_sin_cache, positions, slot_mapping,
+                  kv_cache, errors)
     head = (_cuda(q, torch.bfloat16, "q"), _cuda(q_out, torch.bfloat16, "q_out"),
             _cuda(kv, torch.bfloat16, "kv"), T, H, float(eps),
             _cuda(q_weight, torch.bfloat16, "q_weight"),
@@ -214,12 +254,12 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
     idx = (_cuda(positions, torch.int64, "positions"),
            _cuda(slot_mapping, torch.int64, "slot_mapping"), _cuda(kv_cache, torch.uint8, "kv_cache"))
     if errors is None:
-        st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_out(*head, *idx, kv_cache.shape[1],
-                                                            _stream(stream, q.device))
+        st = _on(dev, lib().dsv4_qnorm_rope_kv_rope_quant_insert_out, *head, *idx,
+                 kv_cache.shape[1], _stream(stream, dev))
     else:
-        st = lib().dsv4_qnorm_rope_kv_rope_quant_insert_checked(
-            *head, cos_sin_cache.shape[0], *idx, kv_cache.shape[0], kv_cache.shape[1],
-            _counter(errors), _stream(stream, q.device))
+        st = _on(dev, lib().dsv4_qnorm_rope_kv_rope_quant_insert_checked,
+                 *head, cos_sin_cache.shape[0], *idx, kv_cache.shape[0], kv_cache.shape[1],
+                 _counter(errors), _stream(stream, dev))
     _check(st, "dsv4_qnorm_rope_kv_rope_quant_insert")
 
 
@@ -234,16 +274,17 @@ def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None, errors=None):
         out = torch.empty((n, DSV4_DIM), dtype=torch.bfloat16, device=kv_cache.device)
     if out.shape != (n, DSV4_DIM):
         raise ValueError("out must be [len(slots), 512]")
+    dev = _device(kv_cache, slots, out, errors)
     if errors is None:
-        st = lib().dsv4_kv_cache_gather(
-            _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1],
-            _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
-            _stream(stream, kv_cache.device))
+        st = _on(dev, lib().dsv4_kv_cache_gather,
+                 _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[1],
+                 _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
+                 _stream(stream, dev))
     else:
-        st = lib().dsv4_kv_cache_gather_checked(
-            _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[0], kv_cache.shape[1],
-            _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
-            _counter(errors), _stream(stream, kv_cache.device))
+        st = _on(dev, lib().dsv4_kv_cache_gather_checked,
+                 _cuda(kv_cache, torch.uint8, "kv_cache"), kv_cache.shape[0], kv_cache.shape[1],
+                 _cuda(slots, torch.int64, "slots"), n, _cuda(out, torch.bfloat16, "out"),
+                 _counter(errors), _stream(stream, dev))
     _check(st, "dsv4_kv_cache_gather")
     return out
 
@@ -281,6 +322,15 @@ def set_stage_wait_limit(polls: int) -> int:
     """Polls of a stage barrier before a warp of a staged QK launch shape
     finishes from global memory (0: always); returns the previous limit."""
     return lib().kvq_set_stage_wait_limit(int(polls))
+
+
+def stage_events(reset: bool = False) -> tuple:
+    """(fallbacks, drain_timeouts) counted by the staged QK launch shapes on
+    the current device since the last reset (waits for the device first)."""
+    fb, dt = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().kvq_stage_events(ctypes.addressof(fb), ctypes.addressof(dt), int(bool(reset))),
+           "kvq_stage_events")
+    return fb.value, dt.value
 
 
 def set_programmatic_launch(enable: bool) -> bool:

@@ -373,6 +373,16 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
 
 uint32_t kvq_set_stage_wait_limit(uint32_t polls) { return kvq::set_stage_wait_limit(polls); }
 
+kvq_status kvq_stage_events(uint64_t* fallbacks, uint64_t* drain_timeouts, int reset) {
+  if (!fallbacks || !drain_timeouts) return KVQ_ERR_NULL;
+  uint64_t v[2] = {0, 0};
+  const cudaError_t e = kvq::stage_events(v, reset != 0);
+  if (e != cudaSuccess) return finish_launch(e);
+  *fallbacks = v[0];
+  *drain_timeouts = v[1];
+  return KVQ_OK;
+}
+
 int kvq_set_programmatic_launch(int enable) {
   return kvq::g_programmatic_launch.exchange(enable != 0, std::memory_order_relaxed) ? 1 : 0;
 }

@@ -81,8 +81,11 @@ int device_sm_count();
 // those of an ordinary launch.
 bool programmatic_launch();
 
-// Launches `kernel` with one by-value parameter block; the launch error is
-// returned (and cleared).
+// Launches `kernel` with one by-value parameter block and returns the
+// launch's own error.  A failed launch's error is taken off the runtime's
+// last-error state (it is reported to the caller instead); after a successful
+// launch that state is left alone, so an error still pending from earlier,
+// unrelated work is not consumed here.
 template <typename Params>
 cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t stream, const Params& p) {
@@ -97,8 +100,8 @@ cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t 
   cfg.attrs = attr;
   cfg.numAttrs = programmatic_launch() ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
-  const cudaError_t last = cudaGetLastError();
-  return e != cudaSuccess ? e : last;
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 constexpr int kMaxDevices = 64;

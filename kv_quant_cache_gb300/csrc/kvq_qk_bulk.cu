@@ -33,7 +33,11 @@
 // times, or for 20 ms, stops staging: it first waits (bounded again) for the
 // copies it still has in flight, then finishes its remaining items with
 // direct global loads, which give the same bits.  A stalled copy costs time,
-// never correctness.
+// never correctness.  Both events are counted in a per-device status word
+// that the host reads (kvq_stage_events): a warp that stopped staging, and a
+// warp whose copies in flight still had not landed when it stopped waiting
+// for them -- its CTA may then exit with a copy still writing its shared
+// memory, which the count makes visible instead of silent.
 #include <atomic>
 #include <cstring>
 
@@ -51,6 +55,11 @@ using Frag4 = qkgen::Frag<4>;
 constexpr int kF = 4;                    // dims per fragment
 constexpr int kUnroll = 4;               // row steps computed together
 using namespace tma;
+
+// Staging events on this device since the last reset: [0] warps that stopped
+// staging because a stage wait ran out, [1] warps whose copies in flight then
+// still had not landed within the drain limit.  Written only on those paths.
+__device__ unsigned long long g_stage_events[2];
 
 struct BulkParams {
   CUtensorMap rows_map;  // tiled launches: [T][Hq + Hk][D] view of the Q/K rows
@@ -223,9 +232,15 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
   if (k < n) {
     // A wait ran out: let the copies still in flight (items k .. k+NS-1)
     // land before this warp's shared memory can be reused, then finish from
-    // global memory.
+    // global memory.  Both events are counted for the host.
+    bool drained = true;
     for (int q = k; q < n && q < k + NS; ++q)
-      mbar_wait_warp(bar0 + 8u * (q % NS), (uint32_t)(q / NS) & 1u, kDrainPolls, kDrainNs);
+      drained &= mbar_wait_warp(bar0 + 8u * (q % NS), (uint32_t)(q / NS) & 1u, kDrainPolls,
+                                kDrainNs);
+    if (lane == 0) {
+      atomicAdd(&g_stage_events[0], 1ull);
+      if (!drained) atomicAdd(&g_stage_events[1], 1ull);
+    }
     for (; k < n; ++k) {
       const Item it = item_at(p, gw + k * nw);
       item_rows<D, NEOX, false>(p, it, g, l, ln, w, global_row<D>(p, it, 0),
@@ -317,6 +332,21 @@ bool qk_bulk_eligible(const QkArgs& a, int shape) {
   chunking(a, kStageBytes[shape] / (2 * a.head_dim), &chunks, &chunk_rows);
   if ((int64_t)(chunks - 1) * chunk_rows >= a.num_heads_q + a.num_heads_k) return false;
   return device_memory(a.qkv) && device_memory(a.cos_sin);
+}
+
+cudaError_t stage_events(uint64_t out[2], bool reset) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  unsigned long long v[2] = {0, 0};
+  e = cudaMemcpyFromSymbol(v, g_stage_events, sizeof v);
+  if (e != cudaSuccess) return e;
+  out[0] = v[0];
+  out[1] = v[1];
+  if (reset) {
+    const unsigned long long zero[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_stage_events, zero, sizeof zero);
+  }
+  return e;
 }
 
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream) {

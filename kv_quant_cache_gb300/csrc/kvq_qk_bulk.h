@@ -29,4 +29,9 @@ bool qk_bulk_eligible(const QkArgs& a, int shape);
 // layout (head_dim 64 / 128 / 256, NeoX or GPT-J, full or partial rotation).
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream);
 
+// The staging-event counters of the current device (kvq_stage_events):
+// waits for the device to finish its work, reads [fallbacks, drain
+// timeouts] and zeroes them if `reset`.
+cudaError_t stage_events(uint64_t out[2], bool reset);
+
 }  // namespace kvq

@@ -123,14 +123,20 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // ---- host side ----------------------------------------------------------------
 
-// True for device memory (the only kind the bulk-copy engine is given).
+// True for memory of the current device (the only kind the bulk-copy engine
+// is given: neither host memory nor another GPU's).  A failed query's error
+// is taken off the runtime's last-error state only if no earlier error was
+// pending there, so an error of other work is never consumed.
 inline bool device_memory(const void* ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const bool clean = cudaPeekAtLastError() == cudaSuccess;
   cudaPointerAttributes attr;
   if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();  // a failed query is not sticky: clear it before the launch
+    if (clean) cudaGetLastError();
     return false;
   }
-  return attr.type == cudaMemoryTypeDevice;
+  return attr.type == cudaMemoryTypeDevice && attr.device == dev;
 }
 
 // cuTensorMapEncodeTiled, fetched once from the driver through the runtime
@@ -146,11 +152,12 @@ inline EncodeTiled encode_tiled() {
   std::call_once(once, [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
+    const bool clean = cudaPeekAtLastError() == cudaSuccess;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiled>(f);
-    else
+    else if (clean)
       cudaGetLastError();
   });
   return fn;

@@ -16,6 +16,8 @@
  *                119, 120, 121, 122, 118, 120, 121 (smallest 2^e with
  *                448 * 2^e >= block max), and q comes out as 1.0.
  *   gather:      reading that entry back gives the block weights exactly.
+ *   errors:      a CUDA error pending in the caller's runtime survives a
+ *                successful call of the library.
  *
  * Exit status 0 when every check holds.
  */
@@ -204,11 +206,25 @@ static void dsv4_case(void) {
   free(cs);
 }
 
+/* An error the caller has pending in its CUDA runtime (here a refused
+ * allocation, which is not sticky) is still there after a successful call of
+ * the library: the library never consumes another party's error. */
+static void pending_error_case(void) {
+  void* huge = NULL;
+  CHECK(cudaMalloc(&huge, (size_t)1 << 62) == cudaErrorMemoryAllocation, "huge allocation");
+  qk_case(128, 1);
+  CHECK(cudaPeekAtLastError() == cudaErrorMemoryAllocation,
+        "the caller's pending error was consumed by a library call");
+  CHECK(cudaGetLastError() == cudaErrorMemoryAllocation, "pending error");
+  CHECK(cudaGetLastError() == cudaSuccess, "error state cleared");
+}
+
 int main(void) {
   for (int st = 0; st <= 6; ++st) CHECK(kvq_status_string((kvq_status)st) != NULL, "status %d", st);
   qk_case(128, 1);  /* head_dim-128 NeoX kernel */
   qk_case(64, 0);   /* general kernel: GPT-J pairs, partial rotation */
   dsv4_case();
+  pending_error_case();
   if (failures) {
     fprintf(stderr, "%d check(s) failed\n", failures);
     return 1;

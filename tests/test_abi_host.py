@@ -281,3 +281,34 @@ def test_programmatic_launch_switch(L):
         assert kvq.set_programmatic_launch(False) is True
     finally:
         kvq.set_programmatic_launch(old)
+
+
+def test_stage_events_rejects_null(L):
+    """The staging-event read-out checks its pointers before touching the
+    device."""
+    x = ctypes.c_uint64(0)
+    assert L.kvq_stage_events(None, ctypes.addressof(x), 0) == kvq.KVQ_ERR_NULL
+    assert L.kvq_stage_events(ctypes.addressof(x), None, 1) == kvq.KVQ_ERR_NULL
+
+
+class _FakeTensor:
+    """Stands in for a tensor in the binding's device check (no GPU here)."""
+
+    def __init__(self, device):
+        self.is_cuda = device >= 0
+        self._device = device
+
+    def get_device(self):
+        return self._device
+
+
+def test_binding_device_check():
+    """Every CUDA tensor of one call must be on one device; pinned host
+    tensors (get_device() == -1) may take part on any; the call runs on the
+    tensors' device."""
+    F = _FakeTensor
+    assert kvq._device(F(1), F(1), None, F(-1)) == 1
+    assert kvq._device(F(-1), F(-1)) == -1
+    assert kvq._device(F(-1), F(3)) == 3
+    with pytest.raises(ValueError, match="same device"):
+        kvq._device(F(0), F(-1), F(1))

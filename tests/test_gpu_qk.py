@@ -10,19 +10,21 @@ from gpu_cases import qk_parity, to_device, with_config
 pytestmark = pytest.mark.gpu
 
 
-def test_decode_size_17_tokens(cuda_device):
+def test_decode_size_17_tokens(cuda_device, parity_log):
     rep = qk_parity(wl.make_qk_workload(wl.QK_SMALL, device=cuda_device))
     assert rep.exact_frac > 0.95
+    parity_log(rep)
 
 
 @pytest.mark.parametrize("config", [-1, 7, 10], ids=["auto", "bulk", "tile"])
-def test_prefill_32768_tokens_every_token(cuda_device, config):
+def test_prefill_32768_tokens_every_token(cuda_device, config, parity_log):
     """The benchmarked workload, compared in full (1,310,720 head rows), under
     the automatic dispatch and under a TMA-staged shape."""
     with with_config("qk", config):
         rep = qk_parity(wl.make_qk_workload(wl.QK_LARGE, device=cuda_device), slice_tokens=8192)
     assert rep.n == 32768 * 40 * 128
     assert rep.exact_frac > 0.95
+    parity_log(rep)
 
 
 @pytest.mark.parametrize("T", [1, 4, 17, 511, 512, 777, 1000, 4096])
@@ -165,15 +167,22 @@ def test_staged_shape_finishing_from_global_memory(cuda_device, config):
     direct loads.  The results are the same bits, and match the oracle."""
     d = wl.make_qk(2000, 32, 8, 8, theta=1e6, max_pos=131072, seed=61, device=cuda_device)
     ref = _run_config(d, 2)
+    kvq.stage_events(reset=True)
+    assert _run_config(d, config).equal(ref)     # default limit: nothing falls back
+    assert kvq.stage_events(reset=True) == (0, 0)
     old = kvq.set_stage_wait_limit(0)
     try:
         assert old > 0
         assert torch.equal(_run_config(d, config), ref)
+        fallbacks, drain_timeouts = kvq.stage_events(reset=True)
+        # every warp with items reports its fallback; each drained its copies
+        assert fallbacks >= 1 and drain_timeouts == 0, (fallbacks, drain_timeouts)
         with with_config("qk", config):
             qk_parity(d)
     finally:
         kvq.set_stage_wait_limit(old)
     assert kvq.set_stage_wait_limit(old) == old
+    assert kvq.stage_events(reset=True)[1] == 0
 
 
 def _run_layout(d, config):
@@ -208,21 +217,46 @@ def test_general_staged_finishing_from_global_memory(cuda_device, layout):
     d = wl.make_qk(900, 16, 4, 4, D=D, theta=1e6, max_pos=131072, seed=D + rot + 1,
                    device=cuda_device, rotary_dim=rot, is_neox=neox)
     ref = _run_layout(d, 5)
+    kvq.stage_events(reset=True)
     old = kvq.set_stage_wait_limit(0)
     try:
         for config in BULK:
             assert torch.equal(_run_layout(d, config), ref), kvq.configs("qk")[config]
+            fallbacks, drain_timeouts = kvq.stage_events(reset=True)
+            assert fallbacks >= 1 and drain_timeouts == 0, (config, fallbacks, drain_timeouts)
     finally:
         kvq.set_stage_wait_limit(old)
 
 
 def test_staged_shape_at_131072_tokens(cuda_device):
     """The largest QK workload of the sweep (131072 tokens, 5.2M head rows:
-    the staged shape's regime), every token against the oracle."""
+    the staged shape's regime), every token against the oracle; no warp
+    stopped staging."""
     d = wl.make_qk(131072, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001, device=cuda_device)
     assert kvq.configs("qk")[kvq.qk_config_for(131072, 32, 8)].startswith("bulk")
+    kvq.stage_events(reset=True)
     rep = qk_parity(d, slice_tokens=16384)
     assert rep.n == 131072 * 40 * 128
+    assert kvq.stage_events(reset=True) == (0, 0)
+
+
+@pytest.mark.skipif(not torch.cuda.is_available() or torch.cuda.device_count() < 2,
+                    reason="needs two GPUs")
+def test_tensors_on_a_device_other_than_the_current_one():
+    """With the current device set to GPU 0, a call on GPU 1's tensors runs
+    on GPU 1 (the binding switches for the call) and matches the oracle; a
+    call mixing the two devices is refused before anything is launched."""
+    dev1 = torch.device("cuda:1")
+    with torch.cuda.device(0):
+        d = wl.make_qk(4096, 32, 8, 8, theta=1e6, max_pos=131072, seed=91, device=dev1)
+        for config in (-1, 7):
+            with with_config("qk", config):
+                qk_parity({k: (v.clone() if isinstance(v, torch.Tensor) else v)
+                           for k, v in d.items()})
+        assert torch.cuda.current_device() == 0
+        with pytest.raises(ValueError):
+            kvq.fused_qk_norm_rope(d["qkv"], 32, 8, 8, 128, d["eps"], d["q_weight"].to("cuda:0"),
+                                   d["k_weight"], d["cos_sin"], True, d["positions"])
 
 
 def test_two_streams_at_once(cuda_device):
@@ -261,7 +295,8 @@ def test_default_stream_is_torchs_current_stream(cuda_device):
     """Calls without `stream` enqueue on torch's current stream, also inside a
     `torch.cuda.stream` context (the binding reads the raw handle)."""
     s = torch.cuda.Stream(cuda_device)
-    assert kvq._stream(None, cuda_device) == torch.cuda.current_stream(cuda_device).cuda_stream
+    idx = cuda_device.index or 0
+    assert kvq._stream(None, idx) == torch.cuda.current_stream(cuda_device).cuda_stream
     with torch.cuda.stream(s):
-        assert kvq._stream(None, cuda_device) == s.cuda_stream
-        assert kvq._stream(None, cuda_device) == torch.cuda.current_stream(cuda_device).cuda_stream
+        assert kvq._stream(None, idx) == s.cuda_stream
+        assert kvq._stream(None, idx) == torch.cuda.current_stream(cuda_device).cuda_stream
