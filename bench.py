@@ -13,8 +13,19 @@ byte the operators must read or write once) / device time of the step, in
 GB/s.  Inputs are resident in HBM and larger than L2 (129 MB), so no L2 flush
 is needed between steps.
 
+The line also carries:
+  * per_config: every workload the benchmark configurations name (the
+    17-token and 32768-token packed-QKV cases, the 16-token and 32768-token
+    DSV4 cases and each point of the DSV4 token sweep), each under the
+    automatic launch shape: median kernel time, GB/s, % of the measured copy
+    peak, and the CPU oracle's GB/s on a token sample of the same workload;
+  * context.unfused_torch: the same two operators of the step as separate
+    eager PyTorch passes on this GPU (RMSNorm, RoPE, and for DSV4 the
+    blockwise scale/cast and the cache scatter), timed and counted with the
+    same algorithmic bytes -- what the fusion saves, not a target.
 --impl reference times the CPU oracle (the only other implementation of this
-path available here) on a bounded sample of the same workload.
+path available here) on the same workload (a token sample only when the
+requested step count would not finish within about a minute).
 --sweep additionally writes per-configuration lines (every workload of the
 parity tests, both launch shapes, the dispatch crossover and a 512 MiB
 device-to-device copy ceiling) to stderr.
@@ -306,28 +317,42 @@ def time_e2e(kvq, qk, ds, steps, device, chunks=8):
 def time_e2e_zero_copy(kvq, qk, ds, steps, device):
     """The step through the C ABI with HOST buffers: the activations and
     indices live in pinned host memory and the kernels read and write them in
-    place over NVLink-C2C (weights, tables and the paged cache stay in HBM).
-    Returns (ms per step, bytes read from host, bytes written to host)."""
+    place over NVLink-C2C (weights and tables stay in HBM).  The paged cache
+    lives in HBM, where attention reads it; every step also copies the whole
+    cache back to pinned host memory (on a second stream, overlapping the next
+    step's QK launch), so the step's written entries reach the host inside
+    the timed region.  Returns (ms per step, bytes read from host, bytes
+    written to host)."""
     hq = {k: v for k, v in qk.items()}
     hd = {k: v for k, v in ds.items()}
     for k in ("qkv", "positions"):
         hq[k] = qk[k].cpu().pin_memory()
     for k in ("q", "kv", "positions", "slot_mapping"):
         hd[k] = ds[k].cpu().pin_memory()
+    cache_host = torch.empty(ds["kv_cache"].shape, dtype=torch.uint8).pin_memory()
     stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
     T = qk["qkv"].shape[0]
     qk_rows = T * (qk["Hq"] + qk["Hk"]) * qk["D"] * 2          # Q and K heads only
     h2d = (qk_rows + T * 8 + hd["q"].numel() * 2 + hd["kv"].numel() * 2 + T * 8 * 2)
-    d2h = qk_rows + hd["q"].numel() * 2
-    launch_qk(kvq, hq, stream)
-    launch_dsv4(kvq, hd, stream)
+    d2h = qk_rows + hd["q"].numel() * 2 + cache_host.numel()
+
+    def one():
+        launch_qk(kvq, hq, stream)
+        stream.wait_stream(side)   # the previous step's cache copy is done before this insert
+        launch_dsv4(kvq, hd, stream)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            cache_host.copy_(ds["kv_cache"], non_blocking=True)
+
+    one()
     torch.cuda.synchronize(device)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(steps):
-        launch_qk(kvq, hq, stream)
-        launch_dsv4(kvq, hd, stream)
+        one()
+    stream.wait_stream(side)
     end.record(stream)
     torch.cuda.synchronize(device)
     return start.elapsed_time(end) / steps, h2d, d2h
@@ -355,6 +380,168 @@ def cpu_baseline(qk, ds, qk_h, ds_h):
     dt = time.perf_counter() - t0
     b_qk, b_ds = step_bytes(qk, ds)
     return (b_qk + b_ds) / dt / 1e9, oracle.default_threads(), dt
+
+
+# ---------------------------------------------------------------------------
+# context: the unfused PyTorch baseline (separate eager passes on the GPU)
+# ---------------------------------------------------------------------------
+
+def unfused_qk(qk):
+    """fused_qk_norm_rope as separate eager PyTorch passes (a comparison
+    baseline, not part of the library): RMSNorm of the Q heads, RMSNorm of
+    the K heads (fp32 results), then NeoX RoPE of each, written back in place
+    as bf16.  Intermediates stay fp32 so the result keeps the operator's
+    single rounding."""
+    T, Hq, Hk, Hv, D = qk["qkv"].shape[0], qk["Hq"], qk["Hk"], qk["Hv"], qk["D"]
+    x = qk["qkv"].view(T, Hq + Hk + Hv, D)
+    cs = qk["cos_sin"].index_select(0, qk["positions"])
+    c, s = cs[:, None, :D // 2], cs[:, None, D // 2:]
+
+    def norm(rows, w):
+        return torch.nn.functional.rms_norm(rows.float(), (D,), w.float(), qk["eps"])
+
+    def rope(n):
+        a, b = n[..., :D // 2], n[..., D // 2:]
+        return torch.cat([a * c - b * s, b * c + a * s], -1)
+
+    nq = norm(x[:, :Hq], qk["q_weight"])
+    nk = norm(x[:, Hq:Hq + Hk], qk["k_weight"])
+    x[:, :Hq] = rope(nq).to(torch.bfloat16)
+    x[:, Hq:Hq + Hk] = rope(nk).to(torch.bfloat16)
+
+
+def unfused_dsv4(ds):
+    """dsv4_qnorm_rope_kv_rope_quant_insert as separate eager PyTorch passes
+    (a comparison baseline, not part of the library): RMSNorm + interleaved
+    RoPE of q (written back in place) and of kv, the blockwise UE8M0 exponent
+    (the smallest e with 448 * 2^e >= amax, from frexp), the e4m3 cast of
+    n * 2^-e, the entry assembled as bytes and scattered into the cache with
+    index_copy_."""
+    q, kv = ds["q"], ds["kv"]
+    T = q.shape[0]
+    cs = ds["cos_sin"].index_select(0, ds["positions"])
+    c, s = cs[:, :32], cs[:, 32:]
+
+    def norm_rope(x, w, cc, ss):
+        n = torch.nn.functional.rms_norm(x.float(), (512,), w.float(), ds["eps"])
+        e, o = n[..., 448::2], n[..., 449::2]
+        n[..., 448:] = torch.stack([e * cc - o * ss, o * cc + e * ss], -1).flatten(-2)
+        return n
+
+    q.copy_(norm_rope(q, ds["q_weight"], c[:, None, :], s[:, None, :]).to(torch.bfloat16))
+    n = norm_rope(kv, ds["kv_weight"], c, s)
+    blocks = n[:, :448].view(T, 7, 64)
+    amax = blocks.abs().amax(-1)
+    mant, ex = torch.frexp(amax)                       # amax = mant * 2^ex, mant in [0.5, 1)
+    e = ex - 9 + (mant > 0.875).to(ex.dtype)           # 448 = 0.875 * 2^9
+    byte = torch.where(amax > 0, (e + 127).clamp(0, 254), torch.zeros_like(e))
+    codes = torch.ldexp(blocks, (127 - byte)[..., None].to(torch.float32))
+    codes = codes.to(torch.float8_e4m3fn).view(torch.uint8).view(T, 448)
+    rope = n[:, 448:].to(torch.bfloat16).contiguous().view(torch.uint8)
+    entry = torch.cat([codes, rope, byte.to(torch.uint8),
+                       torch.zeros((T, 1), dtype=torch.uint8, device=q.device)], -1)
+    slots = ds["slot_mapping"]
+    keep = (slots >= 0).nonzero().squeeze(1)
+    ds["kv_cache"].view(-1, ENTRY).index_copy_(0, slots.index_select(0, keep),
+                                                entry.index_select(0, keep))
+
+
+ENTRY = wl.ENTRY_BYTES
+
+
+def time_unfused(qk, ds, reps, device):
+    """Median ms of each unfused operator on the step's own inputs."""
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    for name, fn, d in (("qk", unfused_qk, qk), ("dsv4", unfused_dsv4, ds)):
+        fn(d)
+        torch.cuda.synchronize(device)
+        med, _ = _time_launch(lambda: fn(d), reps, stream)
+        out[name] = med
+    return out
+
+
+# ---------------------------------------------------------------------------
+# every workload of the benchmark configurations, one record each
+# ---------------------------------------------------------------------------
+
+PER_CONFIG_L2_FLUSH_BELOW = 256 * 2**20
+
+
+def config_workloads():
+    """(config index, operator, workload) for every workload the benchmark
+    configurations name: the packed-QKV decode and prefill cases, the DSV4
+    decode and 32768-token cases, and each point of the DSV4 token sweep."""
+    out = [(0, "qk", wl.QK_SMALL), (1, "qk", wl.QK_LARGE), (2, "dsv4", wl.DSV4_DECODE),
+           (3, "dsv4", wl.DSV4_LARGE)]
+    out += [(4, "dsv4", w) for w in wl.DSV4_SWEEP]
+    return out
+
+
+def oracle_gbs(op, d, sample_tokens):
+    """The CPU oracle's GB/s on the first `sample_tokens` tokens of workload
+    `d` (all host cores), by the same byte count as the GPU figure."""
+    import oracle
+    per_token = ("qkv", "positions") if op == "qk" else ("q", "kv", "positions", "slot_mapping")
+    T = d[per_token[0]].shape[0]
+    S = min(sample_tokens, T)
+
+    def h(k):
+        t = d[k][:S] if k in per_token else d[k]
+        return wl.bf16_bits(t) if t.dtype == torch.bfloat16 else wl.host(t)
+    if op == "qk":
+        args = (h("qkv"), d["Hq"], d["Hk"], d["Hv"], d["D"], d["eps"], h("q_weight"),
+                h("k_weight"), h("cos_sin"), h("positions"))
+        t0 = time.perf_counter()
+        oracle.qk_norm_rope(*args)
+        dt = time.perf_counter() - t0
+        nb = qk_bytes(S, d["Hq"], d["Hk"], d["D"])
+    else:
+        cache = h("kv_cache").copy()
+        slots = h("slot_mapping")
+        args = (h("q"), h("kv"), d["eps"], h("q_weight"), h("kv_weight"), h("cos_sin"),
+                h("positions"), slots, cache)
+        t0 = time.perf_counter()
+        oracle.dsv4(*args)
+        dt = time.perf_counter() - t0
+        nb = dsv4_bytes(S, d["H"], int((slots >= 0).sum()))
+    return nb / dt / 1e9, S
+
+
+def per_config(kvq, device, peak, with_oracle=True, oracle_tokens=2048):
+    """One record per configured workload under the automatic launch shape."""
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
+    recs = []
+    for idx, op, w in config_workloads():
+        if op == "qk":
+            d = wl.make_qk_workload(w, device=device)
+            nb = qk_bytes(w.T, w.Hq, w.Hk, w.D)
+            fn = lambda: launch_qk(kvq, d, stream)  # noqa: E731
+            shape = kvq.configs("qk")[kvq.qk_config_for(w.T, w.Hq, w.Hk)]
+        else:
+            d = wl.make_dsv4_workload(w, device=device)
+            nb = dsv4_bytes(w.T, w.H, int((d["slot_mapping"] >= 0).sum()))
+            fn = lambda: launch_dsv4(kvq, d, stream)  # noqa: E731
+            shape = kvq.configs("dsv4")[kvq.dsv4_config_for(w.T, w.H)]
+        small = nb < PER_CONFIG_L2_FLUSH_BELOW
+        fn()
+        torch.cuda.synchronize(device)
+        reps = 30 if nb < 2**31 else 10
+        med, best = _time_launch(fn, reps, stream, flush if small else None)
+        rec = {"config": idx, "workload": w.name, "launch_shape": shape, "bytes": nb,
+               "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
+               "pct_of_peak": round(100 * nb / med / 1e6 / peak, 2),
+               "l2": "flushed between launches" if small else "larger than L2",
+               "launches": reps}
+        if with_oracle:
+            g, S = oracle_gbs(op, d, oracle_tokens)
+            rec["cpu_oracle_gbs"] = round(g, 3)
+            rec["cpu_oracle_tokens"] = S
+        recs.append(rec)
+        del d
+    del flush
+    return recs
 
 
 def config_block(extra=None):
@@ -392,7 +579,7 @@ def run_gpu(args):
     traffic = recorded_traffic("dsv4_stream_T32768_H64")
     e2e = None
     if not args.no_e2e:
-        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        e2e_steps = max(1, args.steps if args.e2e_steps is None else args.e2e_steps)
         zc_ms, h2d, d2h = time_e2e_zero_copy(kvq, qk, ds, e2e_steps, device)
         zc_ms = max_over_ranks(zc_ms, world, device)
         st_ms, s_h2d, s_d2h, n_chunks = time_e2e(kvq, qk, ds, e2e_steps, device)
@@ -402,12 +589,28 @@ def run_gpu(args):
                "ms_per_step": round(zc_ms, 4), "steps": e2e_steps,
                "path": "C ABI called with pinned host buffers; the kernels read and write "
                        "them in place over NVLink-C2C (host->device / device->host bytes = "
-                       "bytes the kernels read from / write to host memory)",
+                       "bytes the kernels read from / write to host memory); the paged cache "
+                       "(in HBM) is copied back to pinned host memory every step",
                "staged_copies": {"value": round(world * (b_qk + b_ds) / (st_ms * 1e-3) / 1e9, 2),
                                  "ms_per_step": round(st_ms, 4), "h2d_bytes_per_step": s_h2d,
                                  "d2h_bytes_per_step": s_d2h,
                                  "pipeline": f"{n_chunks} token chunks, cudaMemcpyAsync in / "
                                              "kernels / out on three streams"}}
+    context = None
+    per_cfg = None
+    if rank == 0 and not args.no_per_config:
+        unf = time_unfused(qk, ds, 10, device)
+        context = {"unfused_torch": {
+            "what": "the step's two operators as separate eager PyTorch passes on this GPU "
+                    "(rms_norm x2 + RoPE x2 for QK; rms_norm + RoPE of q and kv, blockwise "
+                    "frexp/ldexp/e4m3 cast, entry assembly and index_copy_ for DSV4), fp32 "
+                    "intermediates; GB/s by the same algorithmic bytes as the fused kernels",
+            "qk_ms": round(unf["qk"], 4), "dsv4_ms": round(unf["dsv4"], 4),
+            "qk_gbs": round(b_qk / (unf["qk"] * 1e-3) / 1e9, 1),
+            "dsv4_gbs": round(b_ds / (unf["dsv4"] * 1e-3) / 1e9, 1),
+            "step_gbs": round((b_qk + b_ds) / ((unf["qk"] + unf["dsv4"]) * 1e-3) / 1e9, 1),
+            "fused_speedup": round((unf["qk"] + unf["dsv4"]) / ms_step, 2)}}
+        per_cfg = per_config(kvq, device, peak, with_oracle=host_inputs is not None)
     cpu = None
     if host_inputs is not None:
         v, cores, dt = cpu_baseline(qk, ds, *host_inputs)
@@ -432,6 +635,7 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": b_ds},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+        "per_config": per_cfg, "context": context,
         "dispatch": {"qk": kvq.configs("qk")[kvq.qk_config_for(32768, 32, 8)],
                      "dsv4": kvq.configs("dsv4")[kvq.dsv4_config_for(32768, 64)]},
     }
@@ -448,48 +652,74 @@ def run_gpu(args):
 # reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
 
+def _reference_inputs(S):
+    """Host inputs of the benchmarked step's two workloads at S tokens (the
+    same recipes and seeds, drawn by the CPU generator)."""
+    qk = wl.make_qk(S, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001)
+    ds = wl.make_dsv4(S, 64, max_pos=131072, num_blocks=1024, block_size=64,
+                      slots="perm_prefix", seed=1003)
+    host = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
+            for k, v in {**{"qkv": qk["qkv"], "qw": qk["q_weight"], "kw": qk["k_weight"],
+                            "cs1": qk["cos_sin"], "p1": qk["positions"]},
+                         **{"q": ds["q"], "dqw": ds["q_weight"], "dkw": ds["kv_weight"],
+                            "kv": ds["kv"], "cs2": ds["cos_sin"], "p2": ds["positions"],
+                            "slot": ds["slot_mapping"], "cache": ds["kv_cache"]}}.items()}
+    return host, qk["eps"], ds["eps"]
+
+
+def _reference_step(h, eps_qk, eps_ds):
+    import oracle
+    oracle.qk_norm_rope(h["qkv"], 32, 8, 8, 128, eps_qk, h["qw"], h["kw"], h["cs1"], h["p1"],
+                        out=h["qkv"])
+    oracle.dsv4(h["q"], h["kv"], eps_ds, h["dqw"], h["dkw"], h["cs2"], h["p2"], h["slot"],
+                h["cache"], q_out=h["q"])
+
+
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores,
+    doing the benchmarked step (both operators, all 32768 tokens) per step.
+    Only when K + W such steps would not finish within --reference-budget-s
+    does each step take a token sample of the workload instead (stated in
+    the line)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
-    S = args.cpu_sample_tokens
-    qk = wl.make_qk(S, 32, 8, 8, theta=1e6, max_pos=131072, seed=1001)
-    ds = wl.make_dsv4(S, 64, max_pos=131072, num_blocks=1024, block_size=64,
-                      slots="perm_prefix", seed=1003)
-    qkv = wl.bf16_bits(qk["qkv"])
-    qq = wl.bf16_bits(ds["q"])
-    host = {k: (wl.bf16_bits(v) if v.dtype == torch.bfloat16 else wl.host(v))
-            for k, v in {**{"qw": qk["q_weight"], "kw": qk["k_weight"], "cs1": qk["cos_sin"],
-                            "p1": qk["positions"]},
-                         **{"dqw": ds["q_weight"], "dkw": ds["kv_weight"], "kv": ds["kv"],
-                            "cs2": ds["cos_sin"], "p2": ds["positions"],
-                            "slot": ds["slot_mapping"], "cache": ds["kv_cache"]}}.items()}
-
-    def step():
-        oracle.qk_norm_rope(qkv, 32, 8, 8, 128, qk["eps"], host["qw"], host["kw"], host["cs1"],
-                            host["p1"], out=qkv)
-        oracle.dsv4(qq, host["kv"], ds["eps"], host["dqw"], host["dkw"], host["cs2"], host["p2"],
-                    host["slot"], host["cache"], q_out=qq)
-
+    T = wl.QK_LARGE.T
     warmup = max(args.warmup, 3)
+    S = args.cpu_sample_tokens
+    if S is None:
+        probe, e1, e2 = _reference_inputs(1024)
+        _reference_step(probe, e1, e2)
+        t0 = time.perf_counter()
+        _reference_step(probe, e1, e2)
+        per_token = (time.perf_counter() - t0) / 1024
+        fit = int(args.reference_budget_s / ((args.steps + warmup) * per_token))
+        S = max(64, min(T, fit // 64 * 64))
+        del probe
+    S = max(1, min(S, T))
+    h, eps_qk, eps_ds = _reference_inputs(S)
     for _ in range(warmup):
-        step()
+        _reference_step(h, eps_qk, eps_ds)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        _reference_step(h, eps_qk, eps_ds)
     dt = (time.perf_counter() - t0) / args.steps
     nbytes = qk_bytes(S, 32, 8) + dsv4_bytes(S, 64, S)
     value = nbytes / dt / 1e9
+    sample = ("the whole step: both operators, all 32768 tokens" if S == T else
+              f"first {S} of 32768 tokens of both operators per step (the requested steps "
+              f"at full size would exceed {args.reference_budget_s:.0f} s)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_block({"sample_tokens_per_step": S}),
+        "data": "synthetic",
+        "config": config_block({"tokens_per_step_processed": S, "same_config": S == T,
+                                "l2": "host memory (CPU oracle)"}),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle",
-                         "cores": oracle.default_threads(),
-                         "sample": f"first {S} of 32768 tokens of both operators per step"},
+                         "cores": oracle.default_threads(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -795,10 +1025,16 @@ def main():
     ap.add_argument("--impl", choices=("kvq", "reference"), default="kvq")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end legs (default: --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4096,
-                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload records and the unfused PyTorch context")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=None,
+                    help="tokens per step of the reference (oracle) arm (default: all 32768, "
+                         "fewer only if the requested steps would not finish within "
+                         "--reference-budget-s)")
+    ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--profile", choices=("qk", "dsv4"), default=None)
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--heads", type=int, default=64)

@@ -20,7 +20,7 @@ constexpr int64_t kDefaultDsv4Threshold = 65536;
 // Launch shapes (indices into kDsv4Configs / kQkConfigs) the automatic
 // dispatch uses below / above the threshold.
 constexpr int kDsv4SmallConfig = 0;  // tiles<4w,1row>
-constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg>
+constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg,pairs>
 constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
 constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
 constexpr int kQkStagedConfig = 7;   // bulk<16w,2st,6KB>

@@ -9,14 +9,17 @@
 //   dims 448..511:         the stored bf16 rotary values
 //   slots[i] < 0:          a row of +0.
 //
-// Mapping on sm_103a: a warp per row, lane l reading the entry the way the
-// insert kernel wrote it -- 8 code bytes of chunk 0 (dims 8l..8l+7), 8 of
-// chunk 1 or, on lanes 24..31, 16 bytes of rotary bf16 -- plus the entry's
-// 8-byte exponent word (one broadcast load).  e4m3 -> f16 is exact in
-// hardware; the f16 value times the power of two is exact in fp32; the
-// result is rounded once to bf16.  Entries are 8-byte aligned, so every
-// entry access is an 8-byte load; every output row is two 16-byte stores per
-// lane.
+// Mapping on sm_103a: a warp takes kRows consecutive rows.  Lanes 0..kRows-1
+// load the rows' slots with one coalesced access; then, for every row, lane
+// l reads the entry the way the insert kernel wrote it -- 8 code bytes of
+// chunk 0 (dims 8l..8l+7), 8 of chunk 1 or, on lanes 24..31, 16 bytes of
+// rotary bf16 -- plus the entry's 8-byte exponent word (one broadcast load).
+// All entry loads of the warp's rows are in flight before any is used: a
+// row costs two dependent memory latencies (slot, then entry), which one row
+// per warp could not hide.  e4m3 -> f16 is exact in hardware; the f16 value
+// times the power of two is exact in fp32; the result is rounded once to
+// bf16.  Entries are 8-byte aligned, so every entry access is an 8-byte
+// load; every output row is two 16-byte stores per lane.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -29,6 +32,7 @@ constexpr int kRopeAt = 448;
 constexpr int kScaleAt = 576;
 constexpr int kRopeLane = 24;
 constexpr int kWarps = 8;
+constexpr int kRows = 4;  // rows per warp, all loads in flight together
 
 struct GatherParams {
   const uint8_t* kv_cache;
@@ -59,6 +63,11 @@ __device__ __forceinline__ uint4 dequant8(const uint2 codes, float scale) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One row's entry as held by a lane.
+struct EntryRegs {
+  uint2 scales, c0, c1, r0;
+};
+
 // Checked launches turn a slot that is neither -1 nor inside the cache into a
 // zero row and count it.
 template <bool CHECKED>
@@ -66,37 +75,52 @@ __global__ void __launch_bounds__(kWarps * 32)
 dsv4_gather_kernel(const GatherParams p) {
   grid_dependency_sync();
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (row >= p.num_rows) return;  // whole warp leaves together
-  __nv_bfloat16* dst = p.out + (size_t)row * kDim;
-  const int64_t slot = __ldg(p.slots + row);
-  const bool bad = CHECKED && (slot < -1 || slot >= p.num_slots);
-  if (bad && lane == 0) atomicAdd(p.errors, 1);
-  if (slot < 0 || bad) {
-    store_stream(dst + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
-    store_stream(dst + 256 + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
-    return;
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows;
+  if (row0 >= p.num_rows) return;  // whole warp leaves together
+  const int64_t my_slot = lane < kRows && row0 + lane < p.num_rows ? __ldg(p.slots + row0 + lane)
+                                                                  : -1;
+  int64_t slot[kRows];
+  EntryRegs e[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    slot[r] = __shfl_sync(kFullMask, my_slot, r);
+    const bool bad = CHECKED && (slot[r] < -1 || slot[r] >= p.num_slots);
+    if (bad) {
+      if (lane == 0 && row0 + r < p.num_rows) atomicAdd(p.errors, 1);
+      slot[r] = -1;
+    }
+    if (slot[r] < 0) continue;  // warp-uniform
+    const uint8_t* ent = p.kv_cache + slot[r] * kEntry;
+    e[r].scales = __ldg(reinterpret_cast<const uint2*>(ent + kScaleAt));
+    e[r].c0 = __ldg(reinterpret_cast<const uint2*>(ent + 8 * lane));
+    if (lane < kRopeLane) {
+      e[r].c1 = __ldg(reinterpret_cast<const uint2*>(ent + 256 + 8 * lane));
+    } else {
+      const uint2* rp = reinterpret_cast<const uint2*>(ent + kRopeAt + 16 * (lane - kRopeLane));
+      e[r].c1 = __ldg(rp);
+      e[r].r0 = __ldg(rp + 1);
+    }
   }
-  const uint8_t* ent = p.kv_cache + slot * kEntry;
-  const uint2 scales = __ldg(reinterpret_cast<const uint2*>(ent + kScaleAt));
-  const uint2 c0 = __ldg(reinterpret_cast<const uint2*>(ent + 8 * lane));
-  uint2 c1, r0;
-  if (lane < kRopeLane) {
-    c1 = __ldg(reinterpret_cast<const uint2*>(ent + 256 + 8 * lane));
-  } else {
-    const uint2* rp = reinterpret_cast<const uint2*>(ent + kRopeAt + 16 * (lane - kRopeLane));
-    c1 = __ldg(rp);
-    r0 = __ldg(rp + 1);
-  }
-  const uint32_t b0 = lane >> 3;      // block of chunk 0: 0..3
+  const uint32_t b0 = lane >> 3;        // block of chunk 0: 0..3
   const uint32_t b1 = 4 + (lane >> 3);  // block of chunk 1: 4..6 (lanes < 24)
-  const uint32_t e0 = (b0 < 4 ? scales.x >> (8 * b0) : 0u) & 0xffu;
-  const uint32_t e1 = (b1 < 4 ? scales.x >> (8 * b1) : scales.y >> (8 * (b1 - 4))) & 0xffu;
-  store_stream(dst + 8 * lane, dequant8(c0, ue8m0_scale(e0)));
-  if (lane < kRopeLane) {
-    store_stream(dst + 256 + 8 * lane, dequant8(c1, ue8m0_scale(e1)));
-  } else {  // the rotary dims are stored as bf16 already
-    store_stream(dst + 256 + 8 * lane, make_uint4(c1.x, c1.y, r0.x, r0.y));
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    if (row0 + r >= p.num_rows) break;  // warp-uniform
+    __nv_bfloat16* dst = p.out + (size_t)(row0 + r) * kDim;
+    if (slot[r] < 0) {
+      store_stream(dst + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
+      store_stream(dst + 256 + 8 * lane, make_uint4(0u, 0u, 0u, 0u));
+      continue;
+    }
+    const uint2 sc = e[r].scales;
+    const uint32_t e0 = (sc.x >> (8 * b0)) & 0xffu;
+    const uint32_t e1 = (b1 < 4 ? sc.x >> (8 * b1) : sc.y >> (8 * (b1 - 4))) & 0xffu;
+    store_stream(dst + 8 * lane, dequant8(e[r].c0, ue8m0_scale(e0)));
+    if (lane < kRopeLane) {
+      store_stream(dst + 256 + 8 * lane, dequant8(e[r].c1, ue8m0_scale(e1)));
+    } else {  // the rotary dims are stored as bf16 already
+      store_stream(dst + 256 + 8 * lane, make_uint4(e[r].c1.x, e[r].c1.y, e[r].r0.x, e[r].r0.y));
+    }
   }
 }
 
@@ -110,7 +134,7 @@ cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream) {
   p.num_rows = a.num_rows;
   p.num_slots = a.num_slots;
   p.errors = a.errors;
-  const unsigned grid = (unsigned)((p.num_rows + kWarps - 1) / kWarps);
+  const unsigned grid = (unsigned)((p.num_rows + kWarps * kRows - 1) / (kWarps * kRows));
   return launch_kernel(a.errors != nullptr ? dsv4_gather_kernel<true> : dsv4_gather_kernel<false>,
                        dim3(grid), dim3(kWarps * 32), 0, stream, p);
 }

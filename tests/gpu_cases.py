@@ -64,18 +64,19 @@ def run_dsv4(d):
                                              d["slot_mapping"], d["kv_cache"])
 
 
-def dsv4_parity(d, slice_tokens=2048, sample=None, seed=0):
+def dsv4_parity(d, slice_tokens=2048, sample=None, seed=0, call=None):
     """Run the op on d (GPU tensors) and compare with the oracle.
 
     sample=None: every token, whole cache compared (bytes outside mapped
     entries bit-exact).  sample=n: n tokens (first, last and random ones); the
     sampled tokens' q rows and cache entries are compared, and the rest of the
     cache is checked for the sentinel on the GPU.
+    ``call(d)`` replaces the library call (the unfused baseline's test).
     Returns (q report, cache report)."""
     T = d["q"].shape[0]
     q_in = d["q"].clone()
     cache_in = d["kv_cache"].clone()
-    run_dsv4(d)
+    (call or run_dsv4)(d)
     torch.cuda.synchronize()
     qw, kvw = wl.bf16_bits(d["q_weight"]), wl.bf16_bits(d["kv_weight"])
     cs = wl.host(d["cos_sin"])

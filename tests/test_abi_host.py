@@ -196,6 +196,11 @@ def test_launch_config_table(L):
     finally:
         kvq.set_config("dsv4", -1)
     assert kvq.dsv4_config_for(1, 1) in range(len(kvq.configs("dsv4")))
+    # automatic DSV4 shapes: the one-row grid below the threshold, the
+    # persistent grid taking adjacent row pairs above it
+    ds = kvq.configs("dsv4")
+    assert ds[kvq.dsv4_config_for(16, 64)] == "tiles<4w,1row>"
+    assert ds[kvq.dsv4_config_for(32768, 64)] == "stream<8w,85reg,pairs>"
     assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))
     qk = kvq.configs("qk")
     # automatic QK shapes by Q+K head rows: < 1216 small-batch, < 2^20

@@ -64,7 +64,7 @@ def test_reference_arm_one_line_under_torchrun():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
            "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
-           "--cpu-sample-tokens", "32"]
+           "--reference-budget-s", "1"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -72,3 +72,32 @@ def test_reference_arm_one_line_under_torchrun():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["unit"] == "GB/s" and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+    # a 1 s budget cannot hold four full steps: a token sample, and the line says so
+    S = rec["config"]["tokens_per_step_processed"]
+    assert 64 <= S < 32768 and rec["config"]["same_config"] is False
+    assert f"first {S} of 32768" in rec["cpu_baseline"]["sample"]
+
+
+def test_per_config_covers_every_configured_workload():
+    """One record per workload the benchmark configurations name: the two
+    packed-QKV cases, the two DSV4 cases and the eight sweep points."""
+    ws = bench.config_workloads()
+    assert [i for i, _, _ in ws] == [0, 1, 2, 3] + [4] * 8
+    names = [w.name for _, _, w in ws]
+    assert len(set(names)) == len(names) == 12
+    sweep = [(w.T, w.H) for i, _, w in ws if i == 4]
+    assert sweep == [(1, 128), (17, 128), (1024, 128), (2048, 128), (8192, 128), (32768, 128),
+                     (131072, 128), (131072, 64)]
+
+
+def test_oracle_gbs_on_a_sample():
+    """The per-workload CPU figure: the oracle on a token sample, counted by
+    the same byte model as the GPU figure."""
+    import workloads as wl
+    d = wl.make_dsv4(40, 3, max_pos=4096, num_blocks=4, block_size=32, slots="distinct_skip2",
+                     seed=5)
+    g, S = bench.oracle_gbs("dsv4", d, 16)
+    assert S == 16 and g > 0
+    d = wl.make_qk(20, 4, 2, 2, max_pos=64, seed=6)
+    g, S = bench.oracle_gbs("qk", d, 64)
+    assert S == 20 and g > 0
