@@ -147,7 +147,7 @@ __device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, i
   }
 }
 
-template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED, int G>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED>
 __global__ void __launch_bounds__(WARPS * 32, 1)
 qk_bulk_kernel(const __grid_constant__ BulkParams p) {
   grid_dependency_wait();
@@ -160,14 +160,11 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
   const int g = lane / LPR, l = lane % LPR;
   const int gw = blockIdx.x * WARPS + warp;
   const int nw = gridDim.x * WARPS;
-  // This warp's items: groups of G consecutive items, groups gw, gw + nw, ...;
-  // its k-th item is item_of(k) (k < n).  G > 1 keeps the items a warp has in
-  // flight adjacent in qkv, so the grid reads one contiguous window.
-  const int groups = (p.items + G - 1) / G;
-  if (gw >= groups) return;                     // whole warp leaves together
-  const int ng = (groups - 1 - gw) / nw + 1;
-  const int n = (ng - 1) * G + min(G, p.items - (gw + (ng - 1) * nw) * G);
-  auto item_of = [&](int k) { return (gw + (k / G) * nw) * G + k % G; };
+  // This warp's items: gw + k nw, k < n.  (Giving each warp pairs or quads
+  // of consecutive items instead, so that the items it has in flight are
+  // adjacent, measured 1-5 % slower at every layout and size.)
+  if (gw >= p.items) return;                    // whole warp leaves together
+  const int n = (p.items - 1 - gw) / nw + 1;
 
   uint8_t* ring = smem + (size_t)warp * NS * kStage;
   const uint32_t ring_s = smem_addr(ring);
@@ -189,7 +186,7 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
 
   // Positions of issue window [wb, wb + 32) (one per lane) and of the next.
   auto position = [&](int k) -> int64_t {
-    return k < n ? __ldg(p.positions + item_of(k) / p.chunks) : 0;
+    return k < n ? __ldg(p.positions + (gw + k * nw) / p.chunks) : 0;
   };
   int wb = 0;
   int64_t pos_cur = position(lane), pos_next = position(32 + lane);
@@ -205,7 +202,7 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
     }
     const int64_t pos = __shfl_sync(kFullMask, pos_cur, k - wb);
     if (lane == 0) {
-      const Item it = item_at(p, item_of(k));
+      const Item it = item_at(p, gw + k * nw);
       const uint32_t stage = ring_s + (uint32_t)(k % NS) * kStage;
       const uint32_t bar = bar0 + 8u * (k % NS);
       fence_proxy_async();
@@ -229,7 +226,7 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
     if (!mbar_wait_warp(bar0 + 8u * (k % NS), (uint32_t)(k / NS) & 1u, p.wait_limit, kWaitNs))
       break;
     const uint8_t* stage = ring + (size_t)(k % NS) * kStage;
-    item_rows<D, NEOX, true>(p, item_at(p, item_of(k)), g, l, ln, w,
+    item_rows<D, NEOX, true>(p, item_at(p, gw + k * nw), g, l, ln, w,
                              reinterpret_cast<const __nv_bfloat16*>(stage),
                              reinterpret_cast<const float*>(stage + kCsAt));
     __syncwarp();
@@ -248,7 +245,7 @@ qk_bulk_kernel(const __grid_constant__ BulkParams p) {
       if (!drained) atomicAdd(&g_stage_events[1], 1ull);
     }
     for (; k < n; ++k) {
-      const Item it = item_at(p, item_of(k));
+      const Item it = item_at(p, gw + k * nw);
       item_rows<D, NEOX, false>(p, it, g, l, ln, w, global_row<D>(p, it, 0),
                                 p.cos_sin + __ldg(p.positions + it.t) * p.rot);
     }
@@ -268,12 +265,12 @@ void chunking(const QkArgs& a, int rmax, int* chunks, int* chunk_rows) {
   *chunk_rows = (rows + *chunks - 1) / *chunks;
 }
 
-template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED, int G>
+template <int D, bool NEOX, int WARPS, int NS, int STAGE_BYTES, bool TILED>
 cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
   static_assert(smem_bytes<D, WARPS, NS, STAGE_BYTES>() <= 227 * 1024, "shared memory per CTA");
   static std::atomic<int> cache[kMaxDevices];
   int per_sm = 0;
-  cudaError_t e = prepare(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED, G>,
+  cudaError_t e = prepare(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED>,
                           WARPS * 32, smem_bytes<D, WARPS, NS, STAGE_BYTES>(), cache, &per_sm);
   if (e != cudaSuccess) return e;
   BulkParams p;
@@ -297,30 +294,30 @@ cudaError_t launch_layout(const QkArgs& a, cudaStream_t stream) {
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.row_elems * 2};
     const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)p.chunk_rows, 1};
     if (!encode_bf16_3d(&p.rows_map, p.qkv, dims, strides, box))
-      return launch_layout<D, NEOX, WARPS, NS, STAGE_BYTES, false, G>(a, stream);
+      return launch_layout<D, NEOX, WARPS, NS, STAGE_BYTES, false>(a, stream);
   }
   int64_t grid = (int64_t)per_sm * device_sm_count();
-  const int64_t need = ((p.items + G - 1) / G + WARPS - 1) / WARPS;
+  const int64_t need = (p.items + WARPS - 1) / WARPS;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
-  return launch_kernel(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED, G>,
+  return launch_kernel(qk_bulk_kernel<D, NEOX, WARPS, NS, STAGE_BYTES, TILED>,
                        dim3((unsigned)grid), dim3(WARPS * 32),
                        smem_bytes<D, WARPS, NS, STAGE_BYTES>(), stream, p);
 }
 
-template <int WARPS, int NS, int STAGE_BYTES, bool TILED, int G>
+template <int WARPS, int NS, int STAGE_BYTES, bool TILED>
 cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
   const bool neox = a.is_neox != 0;
   switch (a.head_dim) {
     case 64:
-      return neox ? launch_layout<64, true, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream)
-                  : launch_layout<64, false, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream);
+      return neox ? launch_layout<64, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<64, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
     case 128:
-      return neox ? launch_layout<128, true, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream)
-                  : launch_layout<128, false, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream);
+      return neox ? launch_layout<128, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<128, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
     case 256:
-      return neox ? launch_layout<256, true, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream)
-                  : launch_layout<256, false, WARPS, NS, STAGE_BYTES, TILED, G>(a, stream);
+      return neox ? launch_layout<256, true, WARPS, NS, STAGE_BYTES, TILED>(a, stream)
+                  : launch_layout<256, false, WARPS, NS, STAGE_BYTES, TILED>(a, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -329,7 +326,7 @@ cudaError_t launch_shape(const QkArgs& a, cudaStream_t stream) {
 
 bool qk_bulk_eligible(const QkArgs& a, int shape) {
   static constexpr int kStageBytes[] = {
-#define KVQ_STAGE(W, S, KB, T, G) KB * 1024,
+#define KVQ_STAGE(W, S, KB, T) KB * 1024,
       KVQ_QK_BULK_SHAPES(KVQ_STAGE)
 #undef KVQ_STAGE
   };
@@ -359,7 +356,7 @@ cudaError_t stage_events(uint64_t out[2], bool reset) {
 cudaError_t launch_qk_bulk(const QkArgs& a, int shape, cudaStream_t stream) {
   using Launch = cudaError_t (*)(const QkArgs&, cudaStream_t);
   static constexpr Launch kLaunch[] = {
-#define KVQ_LAUNCH(W, S, KB, T, G) &launch_shape<W, S, KB * 1024, T != 0, G>,
+#define KVQ_LAUNCH(W, S, KB, T) &launch_shape<W, S, KB * 1024, T != 0>,
       KVQ_QK_BULK_SHAPES(KVQ_LAUNCH)
 #undef KVQ_LAUNCH
   };

@@ -10,14 +10,11 @@
 namespace kvq {
 
 // Staged launch shapes X(warps per CTA, stages per warp, KB of head rows per
-// stage, tiled, items per group), in the order of their QK configuration
-// entries (named bulk<Ww,Sst,KKB>, with ",tile" for tiled tensor-map copies
-// and ",G<n>" for shapes whose warps take groups of n consecutive items).  A
-// stage holds KB * 1024 / (2 head_dim) rows plus one cos/sin row.
-#define KVQ_QK_BULK_SHAPES(X)                                                      \
-  X(16, 2, 6, 0, 1) X(24, 2, 3, 0, 1) X(24, 3, 2, 0, 1) X(16, 2, 6, 1, 1) X(16, 2, 6, 0, 2) \
-  X(16, 2, 6, 0, 4)
-#define KVQ_QK_BULK_COUNT(W, S, KB, T, G) +1
+// stage, tiled), in the order of their QK configuration entries (named
+// bulk<Ww,Sst,KKB> and, for tiled tensor-map copies, bulk<Ww,Sst,KKB,tile>).
+// A stage holds KB * 1024 / (2 head_dim) rows plus one cos/sin row.
+#define KVQ_QK_BULK_SHAPES(X) X(16, 2, 6, 0) X(24, 2, 3, 0) X(24, 3, 2, 0) X(16, 2, 6, 1)
+#define KVQ_QK_BULK_COUNT(W, S, KB, T) +1
 constexpr int kQkBulkShapes = 0 KVQ_QK_BULK_SHAPES(KVQ_QK_BULK_COUNT);
 // Index of the first staged shape in the QK configuration table.
 constexpr int kQkFirstBulk = 7;

@@ -251,9 +251,8 @@ cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
 const LaunchConfig kQkConfigs[] = {
     {"tiles<4w,1step>"}, {"tiles<8w,2step>"}, {"tiles<4w,4step>"}, {"tiles<8w,4step>"},
     {"stream<8w,4step>"}, {"general<frag4>"}, {"general<frag8>"},
-#define KVQ_BULK_NAME(W, S, KB, T, G)                                      \
-  {T ? "bulk<" #W "w," #S "st," #KB "KB,tile>"                             \
-     : G > 1 ? "bulk<" #W "w," #S "st," #KB "KB,G" #G ">" : "bulk<" #W "w," #S "st," #KB "KB>"},
+#define KVQ_BULK_NAME(W, S, KB, T) \
+  {T ? "bulk<" #W "w," #S "st," #KB "KB,tile>" : "bulk<" #W "w," #S "st," #KB "KB>"},
     KVQ_QK_BULK_SHAPES(KVQ_BULK_NAME)
 #undef KVQ_BULK_NAME
 };
