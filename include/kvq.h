@@ -132,9 +132,13 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
  *     out_a = n_a * cos_i - n_b * sin_i,   out_b = n_b * cos_i + n_a * sin_i
  * so the partner enters with its own dimension's weight.  head_dim 128 with
  * full NeoX rotation runs tuned register-pipelined kernels, the other
- * layouts a general one; large batches of every layout take a kernel that
- * stages rows through shared memory with the bulk-copy (TMA) engine (launch
- * shapes below).  Every path gives the same bits.
+ * layouts a general one; batches of 128 MiB of Q+K rows and more, in every
+ * layout, take a kernel that stages rows through shared memory with the
+ * bulk-copy (TMA) engine (launch shapes below).  The staged kernel computes
+ * 1/sqrt correctly rounded, the others with the hardware approximation
+ * (within 2 fp32 ulp), each the form it runs fastest with; outputs of the two
+ * are equal but for rare values (about 1 in 10^5), each within the stated
+ * tolerance of the exact result.
  * Source: InfiniOps PR #1019, "Summary" (the API carries is_neox, following
  * vLLM's fused_qk_norm_rope) and "Notes for Reviewers" (the fast path the
  * page guards to: bf16, head_dim 128, full-dimension NeoX).
@@ -282,15 +286,16 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * automatic dispatch picks one by problem size; the override forces one for
  * every later call of the process (benchmark sweeps, tests).  Every DSV4
  * configuration computes bit-identical results.  QK configurations 0-4
- * (register-pipelined) and 7-10 (TMA-staged, bulk<...>) are launch shapes of
- * the head_dim-128 full-NeoX kernels and agree bit for bit; layouts other
- * than that one take the general kernel with 4-dim fragments below 2^19 Q+K
- * rows per call and the staged shape from there on (kvq_qk_config_for
- * describes the head_dim-128 full-NeoX layout).  QK
- * configurations 5 and 6 force the general kernel, with 4- or 8-dim
- * fragments, for every layout; its sum of squares is added in another order,
- * so it agrees with the others within the operator's rounding, not bit for
- * bit.
+ * (register-pipelined shapes of the head_dim-128 full-NeoX kernel) and 5
+ * (the general kernel with 4-dim fragments, any layout) agree bit for bit;
+ * so do configurations 7-10 (TMA-staged, bulk<...>, any layout) among
+ * themselves.  The two groups differ only in the reciprocal square root
+ * (approximate vs correctly rounded; see fused_qk_norm_rope_ex).
+ * Configuration 6 (general, 8-dim fragments) also adds the sum of squares in
+ * another order.  Automatic choice: below 1216 Q+K rows the small-batch
+ * shape, below 128 MiB of Q+K rows (rows x head_dim x 2) the
+ * register-pipelined shape (head_dim 128, full NeoX) or the general kernel,
+ * from there on the staged shape (kvq_qk_config_for describes head_dim 128).
  *   *_num_configs   number of configurations
  *   *_config_name   static name of configuration id (NULL if out of range)
  *   kvq_set_*_config  force id (0 <= id < num) or restore automatic (id < 0);

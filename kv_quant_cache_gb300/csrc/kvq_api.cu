@@ -30,19 +30,18 @@ constexpr int kQkGeneralFrag4Config = 5;
 constexpr int kQkGeneralFrag8Config = 6;
 // Fragment width the general kernel takes for layouts outside the tuned one.
 constexpr int kQkGeneralFrag = 4;
-// Q+K head rows below which the QK operator takes its small-batch shape, and
-// from which it takes the TMA-staged shape (every layout).  Measured on GB300
-// by the benchmark's QK sweeps: at head_dim 128 the staged and the
-// register-pipelined shapes are within a few percent of each other between
-// 160K and 655K rows, the staged shape leads from 1.3M rows on (93 % vs 91 %
-// of the copy peak) and by 11 % at 5.2M rows; for the other layouts it leads
-// the one-shot general kernel by 2-10 % at 650K-1.3M rows.
+// Q+K head rows below which the QK operator takes its small-batch shape.
 constexpr int64_t kQkSmallRows = 152 * 8;
-constexpr int64_t kQkStagedRows = (int64_t)1 << 20;
-// The other layouts' one-shot general kernel gives way to the staged shape
-// earlier (same sweeps: staged 3-13 % faster from 655K rows on at head_dim 64
-// and 256, within a few percent at 330K).
-constexpr int64_t kQkGeneralStagedRows = (int64_t)1 << 19;
+// Bytes of Q+K head rows (rows x head_dim x 2) from which every layout takes
+// the TMA-staged shape; below, the register-pipelined (head_dim 128, full
+// NeoX) or one-shot general kernel.  Measured on GB300 with each launch
+// following a 512 MB write (as the QKV projection precedes this operator):
+// from 160 MB of rows the staged kernel is 6-13 % faster at every layout but
+// one (head_dim 128 with 64 rotated dims: 3 % slower), and ties at 80 MB;
+// it also holds its time after any preceding kernel (111-113 us at 32768
+// tokens x 40 heads), while the one-shot kernels run 106-127 us depending
+// on the L2 contents they start from.
+constexpr int64_t kQkStagedBytes = (int64_t)1 << 27;
 
 std::atomic<int64_t> g_threshold{-1};
 std::atomic<int> g_dsv4_config{-1};
@@ -79,11 +78,13 @@ kvq_status finish_launch(cudaError_t e) {
 
 constexpr int64_t kIndexLimit = (int64_t)1 << 31;
 
-int qk_config_for(int64_t num_tokens, int rows) {
+int qk_config_for(int64_t num_tokens, int rows, int head_dim) {
   const int forced = g_qk_config.load(std::memory_order_relaxed);
   if (forced >= 0) return forced;
   const int64_t n = num_tokens * (int64_t)rows;
-  return n < kQkSmallRows ? kQkSmallConfig : n < kQkStagedRows ? kQkLargeConfig : kQkStagedConfig;
+  return n < kQkSmallRows                        ? kQkSmallConfig
+         : n * head_dim * 2 < kQkStagedBytes ? kQkLargeConfig
+                                                 : kQkStagedConfig;
 }
 
 int dsv4_config_for(int64_t num_tokens, int num_heads) {
@@ -175,9 +176,7 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   const int64_t n = num_tokens * (int64_t)rows;
   const bool small = n < kQkSmallRows;
   const bool tuned = head_dim == 128 && is_neox == 1 && rotary_dim == 128;
-  int config = qk_config_for(num_tokens, rows);
-  if (!tuned && g_qk_config.load(std::memory_order_relaxed) < 0 && n >= kQkGeneralStagedRows)
-    config = kQkStagedConfig;
+  const int config = qk_config_for(num_tokens, rows, head_dim);
   if (config == kQkGeneralFrag4Config || config == kQkGeneralFrag8Config)
     return finish_launch(
         kvq::launch_qk_general(a, small, config == kQkGeneralFrag8Config ? 8 : 4, st));
@@ -396,7 +395,7 @@ const char* kvq_qk_config_name(int id) {
 int kvq_set_qk_config(int id) { return set_config(g_qk_config, id, kvq::kQkNumConfigs); }
 
 int kvq_qk_config_for(int64_t num_tokens, int num_heads_q, int num_heads_k) {
-  return qk_config_for(num_tokens, num_heads_q + num_heads_k);
+  return qk_config_for(num_tokens, num_heads_q + num_heads_k, 128);
 }
 
 int kvq_dsv4_num_configs(void) { return kvq::kDsv4NumConfigs; }

@@ -65,9 +65,16 @@ __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void grid_dependency_sync() {
+// One-shot grids: wait as above, then let the next grid be scheduled -- but
+// only from the CTAs of the grid's last wave (blockIdx.x >= trigger_from, the
+// grid size minus the CTAs the GPU holds at once, computed on the host).  A
+// dependent scheduled while earlier waves are still to come would take SM
+// room from them (measured on GB300: a 32768-token one-shot QK launch
+// followed by a persistent DSV4 launch ran 10 % slower when every CTA
+// triggered at entry).  A grid of one wave triggers from every CTA.
+__device__ __forceinline__ void grid_dependency_sync(int trigger_from) {
   grid_dependency_wait();
-  launch_dependents();
+  if ((int)blockIdx.x >= trigger_from) launch_dependents();
 }
 
 // Streaming 16-byte accesses for data touched exactly once (evict-first).

@@ -66,6 +66,7 @@ struct Dsv4Params {
   int64_t max_pos;    // rows of cos_sin
   int64_t num_slots;  // cache capacity
   int* errors;        // tokens rejected
+  int trigger_from;   // tiles kernel: first CTA of the last wave
 };
 
 // UE8M0 exponent byte (e + 127, clamped to [0, 254]) of the smallest power of
@@ -241,7 +242,7 @@ __device__ __forceinline__ void kv_token(const Dsv4Params& p, int64_t slot, cons
 template <int WARPS, int QROWS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 dsv4_tiles_kernel(const Dsv4Params p) {
-  grid_dependency_sync();
+  grid_dependency_sync(p.trigger_from);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if ((int)blockIdx.x < p.kv_ctas) {
@@ -358,6 +359,7 @@ Dsv4Params make_params(const Dsv4Args& a) {
   p.max_pos = a.max_pos;
   p.num_slots = a.num_slots;
   p.errors = a.errors;
+  p.trigger_from = 0;
   return p;
 }
 
@@ -366,6 +368,9 @@ cudaError_t launch_tiles(const Dsv4Args& a, cudaStream_t stream) {
   Dsv4Params p = make_params(a);
   p.kv_ctas = (p.num_tokens + WARPS - 1) / WARPS;
   const int q_ctas = (p.q_rows + WARPS * QROWS - 1) / (WARPS * QROWS);
+  static std::atomic<int> cache[kMaxDevices];
+  p.trigger_from = last_wave_start(dsv4_tiles_kernel<WARPS, QROWS, MINB, CHECKED>, WARPS * 32,
+                                   p.kv_ctas + q_ctas, cache);
   return launch_kernel(dsv4_tiles_kernel<WARPS, QROWS, MINB, CHECKED>,
                        dim3((unsigned)(p.kv_ctas + q_ctas)), dim3(WARPS * 32), 0, stream, p);
 }
@@ -374,7 +379,9 @@ template <int WARPS, int MINB, bool CHECKED, int G>
 cudaError_t launch_stream(const Dsv4Args& a, cudaStream_t stream) {
   Dsv4Params p = make_params(a);
   int per_sm = 0;
-  cudaError_t e = resident_ctas(dsv4_stream_kernel<WARPS, MINB, CHECKED, G>, WARPS * 32, &per_sm);
+  static std::atomic<int> cache[kMaxDevices];
+  cudaError_t e =
+      resident_ctas(dsv4_stream_kernel<WARPS, MINB, CHECKED, G>, WARPS * 32, cache, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t work_warps = p.q_rows > p.num_tokens ? p.q_rows : p.num_tokens;
   int64_t grid = (int64_t)per_sm * device_sm_count();

@@ -41,6 +41,7 @@ struct GatherParams {
   int num_rows;
   int64_t num_slots;  // bounds-checked launches: cache capacity
   int* errors;        // bounds-checked launches: rows rejected
+  int trigger_from;   // first CTA of the last wave
 };
 
 // 2^(byte - 127) as a binary32 (byte 0 gives the subnormal 2^-127).
@@ -73,7 +74,7 @@ struct EntryRegs {
 template <bool CHECKED>
 __global__ void __launch_bounds__(kWarps * 32)
 dsv4_gather_kernel(const GatherParams p) {
-  grid_dependency_sync();
+  grid_dependency_sync(p.trigger_from);
   const int lane = threadIdx.x & 31;
   const int64_t row0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows;
   if (row0 >= p.num_rows) return;  // whole warp leaves together
@@ -135,8 +136,11 @@ cudaError_t launch_dsv4_gather(const GatherArgs& a, cudaStream_t stream) {
   p.num_slots = a.num_slots;
   p.errors = a.errors;
   const unsigned grid = (unsigned)((p.num_rows + kWarps * kRows - 1) / (kWarps * kRows));
-  return launch_kernel(a.errors != nullptr ? dsv4_gather_kernel<true> : dsv4_gather_kernel<false>,
-                       dim3(grid), dim3(kWarps * 32), 0, stream, p);
+  static std::atomic<int> cache[2][kMaxDevices];
+  const bool checked = a.errors != nullptr;
+  const auto kernel = checked ? dsv4_gather_kernel<true> : dsv4_gather_kernel<false>;
+  p.trigger_from = last_wave_start(kernel, kWarps * 32, grid, cache[checked ? 1 : 0]);
+  return launch_kernel(kernel, dim3(grid), dim3(kWarps * 32), 0, stream, p);
 }
 
 }  // namespace kvq

@@ -106,11 +106,12 @@ cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t 
 
 constexpr int kMaxDevices = 64;
 
-// CTAs of `kernel` that fit on one SM at `threads` threads per CTA, cached
-// per kernel and device (the occupancy query is not free on every launch).
+// CTAs of `kernel` that fit on one SM at `threads` threads per CTA (no
+// dynamic shared memory), cached per device in `cache` -- one cache per
+// kernel, kept by the launcher that owns it (the occupancy query is not free
+// on every launch).
 template <typename Kernel>
-cudaError_t resident_ctas(Kernel kernel, int threads, int* out) {
-  static std::atomic<int> cache[kMaxDevices];
+cudaError_t resident_ctas(Kernel kernel, int threads, std::atomic<int>* cache, int* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -128,6 +129,19 @@ cudaError_t resident_ctas(Kernel kernel, int threads, int* out) {
   if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   *out = n;
   return cudaSuccess;
+}
+
+// First CTA of the last wave of a one-shot launch of `kernel` (grid CTAs of
+// `threads` threads, no dynamic shared memory; occupancy cached in `cache`):
+// the CTAs from there on let the next grid be scheduled
+// (grid_dependency_sync).  0 if the whole grid is resident at once, or if the
+// occupancy query fails.
+template <typename Kernel>
+int last_wave_start(Kernel kernel, int threads, int64_t grid, std::atomic<int>* cache) {
+  int per_sm = 0;
+  if (resident_ctas(kernel, threads, cache, &per_sm) != cudaSuccess) return 0;
+  const int64_t start = grid - (int64_t)per_sm * device_sm_count();
+  return start > 0 ? (int)start : 0;
 }
 
 }  // namespace kvq

@@ -136,8 +136,8 @@ __device__ __forceinline__ void item_rows(const BulkParams& p, const Item& it, i
       if (j0 + RPW * u >= it.nr) break;  // warp-uniform: no row left for any group
       const int j = j0 + RPW * u + g;
       const bool is_q = it.r0 + j < p.num_q;
-      qkgen::row_math<D, kF, NEOX>(xa[u], xb[u], is_q ? w.qa : w.ka, is_q ? w.qb : w.kb, cs, sn,
-                                   ln, p.eps);
+      qkgen::row_math<D, kF, NEOX, true>(xa[u], xb[u], is_q ? w.qa : w.ka, is_q ? w.qb : w.kb, cs,
+                                         sn, ln, p.eps);
       if (j < it.nr) {
         __nv_bfloat16* row = global_row<D>(p, it, j);
         __stcs(reinterpret_cast<uint2*>(row + ln.oa), xa[u]);

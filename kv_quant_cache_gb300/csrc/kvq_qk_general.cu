@@ -38,6 +38,7 @@ struct GenParams {
   float eps;
   int64_t max_pos;  // bounds-checked launches: rows of cos_sin
   int* errors;      // bounds-checked launches: tokens rejected
+  int trigger_from; // first CTA of the last wave
 };
 
 using qkgen::Frag;
@@ -46,7 +47,7 @@ using qkgen::Lane;
 template <int D, int F, int STEPS, bool NEOX, bool CHECKED>
 __global__ void __launch_bounds__(128)
 qk_general_kernel(const GenParams p) {
-  grid_dependency_sync();
+  grid_dependency_sync(p.trigger_from);
   using V = typename Frag<F>::T;
   constexpr int LPR = D / (2 * F);  // lanes per row
   constexpr int RPW = 32 / LPR;     // rows per warp step
@@ -97,7 +98,7 @@ qk_general_kernel(const GenParams p) {
     if (s >= p.steps || first - g + RPW * s >= last) break;  // warp-uniform
     const int h = first + RPW * s;
     const bool is_q = h < p.num_q;
-    qkgen::row_math<D, F, NEOX>(xa[s], xb[s], is_q ? wqa : wka, is_q ? wqb : wkb, cs, sn, ln,
+    qkgen::row_math<D, F, NEOX, false>(xa[s], xb[s], is_q ? wqa : wka, is_q ? wqb : wkb, cs, sn, ln,
                                 p.eps);
     if (h < last) {
       __nv_bfloat16* row = tok + (size_t)h * D;
@@ -128,6 +129,8 @@ cudaError_t launch(const QkArgs& a, cudaStream_t stream) {
   p.steps = (groups + p.chunks - 1) / p.chunks;
   p.items = a.num_tokens * p.chunks;
   const unsigned grid = (unsigned)((p.items + 3) / 4);
+  static std::atomic<int> cache[kMaxDevices];
+  p.trigger_from = last_wave_start(qk_general_kernel<D, F, STEPS, NEOX, CHECKED>, 128, grid, cache);
   return launch_kernel(qk_general_kernel<D, F, STEPS, NEOX, CHECKED>, dim3(grid), dim3(128), 0,
                        stream, p);
 }

@@ -4,8 +4,9 @@
 // "Add the NineToothed NVIDIA implementation of FusedQkNormRope", section
 // "Summary": per-head RMSNorm, then RoPE on the first rotary_dim dims; NeoX
 // pairs (i, i + rotary_dim/2), GPT-J pairs (2i, 2i+1), i < rotary_dim/2).
-// Shared by the one-shot kernel (kvq_qk_general.cu) and the TMA-staged
-// kernel (kvq_qk_bulk.cu), so both give the same bits.
+// Shared by the register-pipelined kernels (kvq_qk_norm_rope.cu), the
+// one-shot general kernel (kvq_qk_general.cu) and the TMA-staged kernel
+// (kvq_qk_bulk.cu).
 //
 // Lane geometry.  A lane holds two fragments of F dims of a row, so a row
 // takes D/(2F) lanes; each of the two load instructions reads a contiguous
@@ -134,25 +135,33 @@ __device__ __forceinline__ void rotate_interleaved(float* v, const float* c, con
   }
 }
 
-// Normalise + rotate one row's fragments in place (xa, xb packed bf16; wa,
-// wb the row's packed weights at the same dims).  All 32 lanes must call it
+// Normalise + rotate one row's fragments in place (xa, xb packed bf16; wa, wb
+// the row's weights at the same dims, as fp32).  All 32 lanes must call it
 // together: the sum of squares is reduced across each row's D/(2F) lanes.
-template <int D, int F, bool NEOX>
-__device__ __forceinline__ void row_math(typename Frag<F>::T& xa, typename Frag<F>::T& xb,
-                                         const typename Frag<F>::T& wpa,
-                                         const typename Frag<F>::T& wpb, const float* cs,
-                                         const float* sn, const Lane<D, F, NEOX>& ln, float eps) {
+// EXACT_RSQRT picks the reciprocal square root: the correctly rounded one,
+// or the hardware approximation (rsqrtf, within 2 fp32 ulp; its error is far
+// below one bf16 ulp of the outputs).  Measured on GB300: the approximation
+// makes the one-shot and register-pipelined kernels 5-13 % faster (they issue
+// an instruction on most cycles), but the TMA-staged kernel 8-12 % slower
+// (its schedule around the copies changes), so each takes its faster form.
+// Kernels on the same form give the same bits; across the two forms an
+// output can differ in its last bit where the fp32 value lies next to a bf16
+// rounding boundary.
+template <int D, int F, bool NEOX, bool EXACT_RSQRT>
+__device__ __forceinline__ void row_math_w(typename Frag<F>::T& xa, typename Frag<F>::T& xb,
+                                           const float* wa, const float* wb, const float* cs,
+                                           const float* sn, const Lane<D, F, NEOX>& ln,
+                                           float eps) {
   constexpr int LPR = D / (2 * F);
-  float a[F], b[F], wa[F], wb[F];
+  float a[F], b[F];
   Frag<F>::unpack(xa, a);
   Frag<F>::unpack(xb, b);
   float ss = 0.0f;
 #pragma unroll
   for (int k = 0; k < F; ++k) ss = fmaf(b[k], b[k], fmaf(a[k], a[k], ss));
   ss = group_sum<LPR>(ss);
-  const float r = __frsqrt_rn(ss * (1.0f / D) + eps);
-  Frag<F>::unpack(wpa, wa);
-  Frag<F>::unpack(wpb, wb);
+  const float v = ss * (1.0f / D) + eps;
+  const float r = EXACT_RSQRT ? __frsqrt_rn(v) : rsqrtf(v);
   float na[F], nb[F];
 #pragma unroll
   for (int k = 0; k < F; ++k) {
@@ -174,6 +183,18 @@ __device__ __forceinline__ void row_math(typename Frag<F>::T& xa, typename Frag<
   }
   xa = Frag<F>::pack(na);
   xb = Frag<F>::pack(nb);
+}
+
+// The same with the weights packed as bf16 (widened here).
+template <int D, int F, bool NEOX, bool EXACT_RSQRT>
+__device__ __forceinline__ void row_math(typename Frag<F>::T& xa, typename Frag<F>::T& xb,
+                                         const typename Frag<F>::T& wpa,
+                                         const typename Frag<F>::T& wpb, const float* cs,
+                                         const float* sn, const Lane<D, F, NEOX>& ln, float eps) {
+  float wa[F], wb[F];
+  Frag<F>::unpack(wpa, wa);
+  Frag<F>::unpack(wpb, wb);
+  row_math_w<D, F, NEOX, EXACT_RSQRT>(xa, xb, wa, wb, cs, sn, ln, eps);
 }
 
 }  // namespace qkgen

@@ -54,6 +54,7 @@ struct QkParams {
   float eps;
   int64_t max_pos;    // bounds-checked launches: rows of cos_sin
   int* errors;        // bounds-checked launches: tokens rejected
+  int trigger_from;   // one-shot launches: first CTA of the last wave
 };
 
 // Weight fragments of this lane (dims [4l, 4l+4) and [64+4l, 64+4l+4), Q and
@@ -81,7 +82,7 @@ __device__ __forceinline__ void row_math(uint2& lo, uint2& hi, bool is_q, const 
   const float c[4] = {c4.x, c4.y, c4.z, c4.w};
   const float s[4] = {s4.x, s4.y, s4.z, s4.w};
   const qkgen::Lane<kHeadDim, 4, true> full(0, kHeadDim);  // both fragments rotated
-  qkgen::row_math<kHeadDim, 4, true>(lo, hi, is_q ? w.q_lo : w.k_lo, is_q ? w.q_hi : w.k_hi, c, s,
+  qkgen::row_math<kHeadDim, 4, true, false>(lo, hi, is_q ? w.q_lo : w.k_lo, is_q ? w.q_hi : w.k_hi, c, s,
                                      full, eps);
 }
 
@@ -176,7 +177,7 @@ __device__ __forceinline__ void do_item(const QkParams& p, int item, int half, i
 template <int WARPS, int STEPS, int MINB, bool CHECKED>
 __global__ void __launch_bounds__(WARPS * 32, MINB)
 qk_tiles_kernel(const QkParams p) {
-  grid_dependency_sync();
+  grid_dependency_sync(p.trigger_from);
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (item >= p.items) return;  // whole warp leaves together
@@ -217,21 +218,26 @@ QkParams make_params(const QkArgs& a, int steps) {
   p.eps = a.eps;
   p.max_pos = a.max_pos;
   p.errors = a.errors;
+  p.trigger_from = 0;
   return p;
 }
 
 template <int WARPS, int STEPS, int MINB, bool CHECKED = false>
 cudaError_t launch_tiles(const QkArgs& a, cudaStream_t stream) {
-  const QkParams p = make_params(a, STEPS);
+  QkParams p = make_params(a, STEPS);
   const unsigned grid = (unsigned)((p.items + WARPS - 1) / WARPS);
+  static std::atomic<int> cache[kMaxDevices];
+  p.trigger_from =
+      last_wave_start(qk_tiles_kernel<WARPS, STEPS, MINB, CHECKED>, WARPS * 32, grid, cache);
   return launch_kernel(qk_tiles_kernel<WARPS, STEPS, MINB, CHECKED>, dim3(grid), dim3(WARPS * 32),
                        0, stream, p);
 }
 
 template <typename Kernel>
-cudaError_t launch_persistent(Kernel kernel, const QkParams& p, int warps, cudaStream_t stream) {
+cudaError_t launch_persistent(Kernel kernel, const QkParams& p, int warps,
+                              std::atomic<int>* cache, cudaStream_t stream) {
   int per_sm = 0;
-  cudaError_t e = resident_ctas(kernel, warps * 32, &per_sm);
+  cudaError_t e = resident_ctas(kernel, warps * 32, cache, &per_sm);
   if (e != cudaSuccess) return e;
   int64_t grid = (int64_t)per_sm * device_sm_count();
   const int64_t need = (p.items + warps - 1) / warps;
@@ -242,8 +248,9 @@ cudaError_t launch_persistent(Kernel kernel, const QkParams& p, int warps, cudaS
 
 template <int WARPS, int STEPS, int MINB>
 cudaError_t launch_stream(const QkArgs& a, cudaStream_t stream) {
+  static std::atomic<int> cache[kMaxDevices];
   return launch_persistent(qk_stream_kernel<WARPS, STEPS, MINB>, make_params(a, STEPS), WARPS,
-                           stream);
+                           cache, stream);
 }
 
 }  // namespace

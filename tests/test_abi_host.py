@@ -203,13 +203,13 @@ def test_launch_config_table(L):
     assert ds[kvq.dsv4_config_for(32768, 64)] == "stream<8w,85reg,pairs>"
     assert kvq.qk_config_for(32768, 32, 8) in range(len(kvq.configs("qk")))
     qk = kvq.configs("qk")
-    # automatic QK shapes by Q+K head rows: < 1216 small-batch, < 2^20
-    # register-pipelined, from there on TMA-staged
+    # automatic QK shapes at head_dim 128: < 1216 Q+K rows small-batch,
+    # < 128 MiB of Q+K rows (2^19 rows) register-pipelined, then TMA-staged
     assert qk[kvq.qk_config_for(17, 16, 8)] == "tiles<4w,1step>"
     assert qk[kvq.qk_config_for(30, 32, 8)] == "tiles<4w,1step>"   # 1200 rows
     assert qk[kvq.qk_config_for(31, 32, 8)] == "tiles<4w,4step>"   # 1240 rows
-    assert qk[kvq.qk_config_for(26214, 32, 8)] == "tiles<4w,4step>"   # 1048560 rows
-    assert qk[kvq.qk_config_for(26215, 32, 8)] == "bulk<16w,2st,6KB>"
+    assert qk[kvq.qk_config_for(13107, 32, 8)] == "tiles<4w,4step>"   # 524280 rows
+    assert qk[kvq.qk_config_for(13108, 32, 8)] == "bulk<16w,2st,6KB>"
     assert qk[kvq.qk_config_for(32768, 32, 8)] == "bulk<16w,2st,6KB>"
 
 
