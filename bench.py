@@ -556,6 +556,79 @@ def per_config(kvq, device, peak, with_oracle=True, oracle_tokens=2048):
     return recs
 
 
+# ---------------------------------------------------------------------------
+# the rows beyond the two operators' benchmarked layouts: cache read-back,
+# other QK layouts, decode steps in a CUDA graph
+# ---------------------------------------------------------------------------
+
+def next_rows(kvq, device, peak):
+    """One record per measured extension: dsv4_kv_cache_gather on random
+    slots of a full 65536-slot cache; fused_qk_norm_rope at head_dim 64 and
+    256 and with partial or GPT-J rotation; a 32-layer decode step (QK 17
+    tokens + DSV4 16 tokens x 64 heads per layer) replayed as one CUDA graph."""
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
+    recs = []
+    d = wl.make_dsv4_workload(wl.DSV4_LARGE, device=device)
+    launch_dsv4(kvq, d, stream)
+    for n in (16, 32768, 131072):
+        slots = torch.randint(0, 65536, (n,), device=device, dtype=torch.int64,
+                              generator=torch.Generator(device=device).manual_seed(n))
+        rows = torch.empty((n, 512), dtype=torch.bfloat16, device=device)
+        nb = n * (584 + 8 + 1024)
+        fn = lambda: kvq.dsv4_kv_cache_gather(d["kv_cache"], slots, rows, stream)  # noqa: E731
+        fn()
+        med, _ = _time_launch(fn, 30, stream, flush)
+        recs.append({"row": "f2 dsv4_kv_cache_gather", "rows": n, "bytes": nb,
+                     "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
+                     "pct_of_peak": round(100 * nb / med / 1e6 / peak, 2),
+                     "l2": "flushed between launches"})
+    del d
+    for T, D, rot, neox in ((32768, 64, 64, True), (32768, 64, 32, False), (32768, 128, 64, True),
+                            (32768, 128, 128, False), (16384, 256, 256, True),
+                            (16384, 256, 64, False)):
+        q = wl.make_qk(T, 32, 8, 8, D=D, theta=1e6, max_pos=131072, seed=D + rot, device=device,
+                       rotary_dim=rot, is_neox=neox)
+        nb = qk_bytes(T, 32, 8, D, rot)
+        fn = lambda: kvq.fused_qk_norm_rope(q["qkv"], 32, 8, 8, D, q["eps"], q["q_weight"],  # noqa: E731
+                                            q["k_weight"], q["cos_sin"], neox, q["positions"],
+                                            stream=stream, rotary_dim=rot)
+        fn()
+        med, _ = _time_launch(fn, 30, stream, flush)
+        recs.append({"row": "f1 fused_qk_norm_rope_ex", "tokens": T, "heads": [32, 8, 8],
+                     "head_dim": D, "rotary_dim": rot, "pairs": "neox" if neox else "gptj",
+                     "bytes": nb, "us_median": round(med * 1e3, 2), "gbs": round(nb / med / 1e6, 1),
+                     "pct_of_peak": round(100 * nb / med / 1e6 / peak, 2),
+                     "l2": "flushed between launches (each launch follows a 512 MB write)"})
+        del q
+    layers = []
+    for i in range(32):
+        q = wl.make_qk(17, 16, 8, 8, theta=1e4, max_pos=4096, seed=i, device=device)
+        ds = wl.make_dsv4(16, 64, max_pos=65536, num_blocks=64, block_size=64,
+                          slots="distinct_skip2", seed=i, device=device)
+        layers.append((q, ds))
+
+    def decode(st):
+        for q, ds in layers:
+            launch_qk(kvq, q, st)
+            launch_dsv4(kvq, ds, st)
+    decode(stream)
+    torch.cuda.synchronize(device)
+    eager_ms, _ = _time_launch(lambda: decode(stream), 20, stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode(torch.cuda.current_stream(device))
+    graph.replay()
+    torch.cuda.synchronize(device)
+    graph_ms, _ = _time_launch(graph.replay, 20, stream)
+    recs.append({"row": "f3 decode step in a CUDA graph", "layers": 32,
+                 "launches": 64, "eager_us": round(eager_ms * 1e3, 1),
+                 "graph_us": round(graph_ms * 1e3, 1),
+                 "graph_us_per_launch": round(graph_ms * 1e3 / 64, 2)})
+    del graph, layers, flush
+    return recs
+
+
 def config_block(extra=None):
     c = {"workload": "fused_qk_norm_rope T=32768 Hq/Hk/Hv=32/8/8 D=128 theta=1e6 + "
                      "dsv4_qnorm_rope_kv_rope_quant_insert T=32768 H=64 (65536-slot cache)",
@@ -610,6 +683,7 @@ def run_gpu(args):
                                              "kernels / out on three streams"}}
     context = None
     per_cfg = None
+    nexts = None
     if rank == 0 and not args.no_per_config:
         unf = time_unfused(qk, ds, 10, device)
         context = {"unfused_torch": {
@@ -623,6 +697,7 @@ def run_gpu(args):
             "step_gbs": round((b_qk + b_ds) / ((unf["qk"] + unf["dsv4"]) * 1e-3) / 1e9, 1),
             "fused_speedup": round((unf["qk"] + unf["dsv4"]) / ms_step, 2)}}
         per_cfg = per_config(kvq, device, peak, with_oracle=host_inputs is not None)
+        nexts = next_rows(kvq, device, peak)
     cpu = None
     if host_inputs is not None:
         v, cores, dt = cpu_baseline(qk, ds, *host_inputs)
@@ -652,7 +727,7 @@ def run_gpu(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
         "gpu_launches_note": "launches in the timed region; the per-kernel pass launches as "
                              "many again",
-        "per_config": per_cfg, "context": context,
+        "per_config": per_cfg, "next_rows": nexts, "context": context,
         "dispatch": {"qk": kvq.configs("qk")[kvq.qk_config_for(32768, 32, 8)],
                      "dsv4": kvq.configs("dsv4")[kvq.dsv4_config_for(32768, 64)]},
     }

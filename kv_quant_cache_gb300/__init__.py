@@ -157,21 +157,24 @@ def _stream(stream, device) -> int:
     return int(stream)
 
 
-_current_device = torch.cuda.current_device
+# The current device as torch's runtime sees it (the raw query, without the
+# public API's lazy-initialisation check; the public API is the fallback).
+_current_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
 
 
 def _device(*tensors) -> int:
     """The one CUDA device that every CUDA tensor of a call is on (pinned host
-    tensors may take part on any device); -1 if none is a CUDA tensor."""
+    tensors, whose get_device() is -1, may take part on any device); -1 if
+    none is a CUDA tensor."""
     dev = -1
     for t in tensors:
-        if t is not None and t.is_cuda:
+        if t is not None:
             d = t.get_device()
-            if dev < 0:
+            if d != dev and d >= 0:
+                if dev >= 0:
+                    raise ValueError(f"tensors on cuda:{dev} and cuda:{d}: every CUDA tensor "
+                                     "of one call must be on the same device")
                 dev = d
-            elif d != dev:
-                raise ValueError(f"tensors on cuda:{dev} and cuda:{d}: every CUDA tensor of "
-                                 "one call must be on the same device")
     return dev
 
 
