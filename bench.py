@@ -18,7 +18,9 @@ The line also carries:
     17-token and 32768-token packed-QKV cases, the 16-token and 32768-token
     DSV4 cases and each point of the DSV4 token sweep), each under the
     automatic launch shape: median kernel time, GB/s, % of the measured copy
-    peak, and the CPU oracle's GB/s on a token sample of the same workload;
+    peak, the time of a plain device copy moving the same bytes (the copy
+    ceiling at that launch length), and the CPU oracle's GB/s on a token
+    sample of the same workload;
   * context.unfused_torch: the same two operators of the step as separate
     eager PyTorch passes on this GPU (RMSNorm, RoPE, and for DSV4 the
     blockwise scale/cast and the cache scatter), timed and counted with the
@@ -546,6 +548,15 @@ def per_config(kvq, device, peak, with_oracle=True, oracle_tokens=2048):
                "pct_of_peak": round(100 * nb / med / 1e6 / peak, 2),
                "l2": "flushed between launches" if small else "larger than L2",
                "launches": reps}
+        # the copy ceiling at this launch length: a plain device copy moving
+        # the same bytes (half read, half written), timed the same way
+        src = torch.empty(nb // 2, dtype=torch.uint8, device=device)
+        dst = torch.empty_like(src)
+        dst.copy_(src)
+        cmed, _ = _time_launch(lambda: dst.copy_(src), reps, stream, flush if small else None)
+        rec["copy_us_median"] = round(cmed * 1e3, 2)
+        rec["pct_of_copy"] = round(100 * cmed / med, 1)
+        del src, dst
         if with_oracle:
             g, S = oracle_gbs(op, d, oracle_tokens)
             rec["cpu_oracle_gbs"] = round(g, 3)
@@ -1090,10 +1101,16 @@ def sweep(kvq, device):
 
 def run_profile_case(args):
     """A reduced case of one kernel for profiler captures: --profile qk|dsv4,
-    --tokens T, --heads H, --launches n (each launch on the same inputs)."""
+    --tokens T, --heads H, --launches n (each launch on the same inputs),
+    --shape NAME (a launch shape by its name; default: the automatic one)."""
     import kv_quant_cache_gb300 as kvq
     device = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(device)
+    if args.shape is not None:
+        names = kvq.configs(args.profile)
+        if args.shape not in names:
+            raise SystemExit(f"--shape: {args.shape!r} is not one of {names}")
+        kvq.set_config(args.profile, names.index(args.shape))
     if args.profile == "qk":
         d = wl.make_qk(args.tokens, args.heads, 8, 8, theta=1e6, max_pos=131072, seed=1001,
                        device=device)
@@ -1131,6 +1148,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=4096)
     ap.add_argument("--heads", type=int, default=64)
     ap.add_argument("--launches", type=int, default=5)
+    ap.add_argument("--shape", default=None)
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)

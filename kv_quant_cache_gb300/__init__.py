@@ -29,6 +29,7 @@ KVQ_ERR_VALUE = 6
 
 ENTRY_BYTES = 584
 DSV4_DIM = 512
+DSV4_ROPE_DIM = 64  # rotated dims of a DSV4 row: cos/sin table width
 
 
 class KvqError(RuntimeError):
@@ -213,6 +214,10 @@ def fused_qk_norm_rope(qkv, num_heads_q, num_heads_k, num_heads_v, head_dim, eps
     if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != rotary_dim:
         raise ValueError("cos_sin_cache must be [max_pos, rotary_dim]")
     T = qkv.shape[0]
+    if q_weight.numel() != head_dim or k_weight.numel() != head_dim:
+        raise ValueError("q_weight and k_weight must hold head_dim values")
+    if positions.numel() != T:
+        raise ValueError("positions must hold one value per token")
     dev = _device(qkv, q_weight, k_weight, cos_sin_cache, positions, errors)
     args = (_cuda(qkv, torch.bfloat16, "qkv"), T, num_heads_q, num_heads_k, num_heads_v,
             head_dim, float(eps), _cuda(q_weight, torch.bfloat16, "q_weight"),
@@ -247,6 +252,12 @@ def dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, eps, q_weight, kv_weight, cos_si
         q_out = q
     if q_out.shape != q.shape:
         raise ValueError("q_out must have q's shape")
+    if q_weight.numel() != DSV4_DIM or kv_weight.numel() != DSV4_DIM:
+        raise ValueError("q_weight and kv_weight must hold 512 values")
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != DSV4_ROPE_DIM:
+        raise ValueError("cos_sin_cache must be [max_pos, 64]")
+    if positions.numel() != T or slot_mapping.numel() != T:
+        raise ValueError("positions and slot_mapping must hold one value per token")
     dev = _device(q, q_out, kv, q_weight, kv_weight, cos_sin_cache, positions, slot_mapping,
                   kv_cache, errors)
     head = (_cuda(q, torch.bfloat16, "q"), _cuda(q_out, torch.bfloat16, "q_out"),
@@ -272,6 +283,8 @@ def dsv4_kv_cache_gather(kv_cache, slots, out=None, stream=None, errors=None):
     ``errors`` (int32 CUDA tensor) selects the bounds-checked launch."""
     if kv_cache.dim() != 3 or kv_cache.shape[2] != ENTRY_BYTES:
         raise ValueError("kv_cache must be [num_blocks, block_size, 584]")
+    if slots.dim() != 1:
+        raise ValueError("slots must be a 1-D int64 tensor")
     n = slots.shape[0]
     if out is None:
         out = torch.empty((n, DSV4_DIM), dtype=torch.bfloat16, device=kv_cache.device)

@@ -78,10 +78,11 @@ kvq_status finish_launch(cudaError_t e) {
 
 constexpr int64_t kIndexLimit = (int64_t)1 << 31;
 
-int qk_config_for(int64_t num_tokens, int rows, int head_dim) {
+int qk_config_for(int64_t num_tokens, int64_t rows, int head_dim) {
   const int forced = g_qk_config.load(std::memory_order_relaxed);
   if (forced >= 0) return forced;
-  const int64_t n = num_tokens * (int64_t)rows;
+  if (num_tokens >= kIndexLimit || rows >= kIndexLimit) return kQkStagedConfig;
+  const int64_t n = num_tokens * rows;
   return n < kQkSmallRows                        ? kQkSmallConfig
          : n * head_dim * 2 < kQkStagedBytes ? kQkLargeConfig
                                                  : kQkStagedConfig;
@@ -148,9 +149,12 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   if (rotary_dim < 16 || rotary_dim > head_dim || rotary_dim % 16 != 0)
     return KVQ_ERR_UNSUPPORTED;
   if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
-  const int rows = num_heads_q + num_heads_k;
-  if ((int64_t)rows + num_heads_v > (1 << 20) || num_tokens * (int64_t)(rows + 1) >= kIndexLimit)
+  // head counts summed in 64 bits: each is at most INT_MAX
+  const int64_t rows64 = (int64_t)num_heads_q + num_heads_k;
+  if (rows64 + num_heads_v > (1 << 20) || num_tokens >= kIndexLimit ||
+      num_tokens * (rows64 + 1) >= kIndexLimit)
     return KVQ_ERR_SHAPE;
+  const int rows = (int)rows64;
   if (num_tokens == 0 || rows == 0) return KVQ_OK;
   if (!qkv || !q_weight || !k_weight || !cos_sin_cache || !positions) return KVQ_ERR_NULL;
   if (!aligned(qkv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) ||
@@ -195,7 +199,8 @@ kvq_status dsv4_impl(const void* q, void* q_out, const void* kv, int64_t num_tok
                      int64_t max_pos, int64_t num_slots, int32_t* errors,
                      kvq_stream_t stream) {
   if (num_tokens < 0 || num_heads < 1 || block_size < 1) return KVQ_ERR_SHAPE;
-  if (num_tokens * (int64_t)(num_heads + 1) >= kIndexLimit) return KVQ_ERR_SHAPE;
+  if (num_tokens >= kIndexLimit || num_tokens * ((int64_t)num_heads + 1) >= kIndexLimit)
+    return KVQ_ERR_SHAPE;
   if (!std::isfinite(eps) || eps < 0.0f) return KVQ_ERR_VALUE;
   if (num_tokens == 0) return KVQ_OK;
   if (!q || !q_out || !kv || !q_weight || !kv_weight || !cos_sin_cache || !positions ||
@@ -367,7 +372,8 @@ int64_t kvq_set_dsv4_dispatch_threshold(int64_t value) {
 }
 
 int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads) {
-  return num_tokens * (int64_t)(num_heads + 1) < current_threshold() ? 0 : 1;
+  if (num_tokens >= kIndexLimit) return 1;  // keeps the product below from overflowing
+  return num_tokens * ((int64_t)num_heads + 1) < current_threshold() ? 0 : 1;
 }
 
 uint32_t kvq_set_stage_wait_limit(uint32_t polls) { return kvq::set_stage_wait_limit(polls); }
@@ -395,7 +401,7 @@ const char* kvq_qk_config_name(int id) {
 int kvq_set_qk_config(int id) { return set_config(g_qk_config, id, kvq::kQkNumConfigs); }
 
 int kvq_qk_config_for(int64_t num_tokens, int num_heads_q, int num_heads_k) {
-  return qk_config_for(num_tokens, num_heads_q + num_heads_k, 128);
+  return qk_config_for(num_tokens, (int64_t)num_heads_q + num_heads_k, 128);
 }
 
 int kvq_dsv4_num_configs(void) { return kvq::kDsv4NumConfigs; }

@@ -107,6 +107,12 @@ def test_qk_validation(L):
     assert qk(L, cs=MIS) == kvq.KVQ_ERR_ALIGN
     assert qk(L, pos=A16 + 4) == kvq.KVQ_ERR_ALIGN
     assert qk(L, T=1 << 30, hq=2, hk=0) == kvq.KVQ_ERR_SHAPE   # index range
+    # sums and products that overflow 32 or 64 bits are rejected, not wrapped
+    INT_MAX = 2**31 - 1
+    assert qk(L, hq=INT_MAX, hk=INT_MAX, hv=0) == kvq.KVQ_ERR_SHAPE
+    assert qk(L, hq=INT_MAX, hk=1, hv=INT_MAX) == kvq.KVQ_ERR_SHAPE
+    assert qk(L, T=2**62, hq=4, hk=0) == kvq.KVQ_ERR_SHAPE
+    assert qk(L, T=2**63 - 1, hq=1, hk=0, hv=0) == kvq.KVQ_ERR_SHAPE
     # nothing to do: OK without a launch, even with NULL pointers
     assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, T=0) == kvq.KVQ_OK
     assert qk(L, qkv=None, qw=None, kw=None, cs=None, pos=None, hq=0, hk=0) == kvq.KVQ_OK
@@ -124,6 +130,11 @@ def test_dsv4_validation(L):
     assert dsv4(L, H=0) == kvq.KVQ_ERR_SHAPE
     assert dsv4(L, bs=0) == kvq.KVQ_ERR_SHAPE
     assert dsv4(L, T=1 << 24, H=128) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, T=1, H=2**31 - 1) == kvq.KVQ_ERR_SHAPE
+    assert dsv4(L, T=2**62, H=3) == kvq.KVQ_ERR_SHAPE
+    assert L.kvq_dsv4_dispatch_path(2**62, 3) == 1
+    assert L.kvq_dsv4_dispatch_path(1, 2**31 - 1) == 1
+    assert L.kvq_qk_config_for(2**62, 3, 1) == L.kvq_qk_config_for(1 << 20, 32, 8)
     assert dsv4(L, eps=float("nan")) == kvq.KVQ_ERR_VALUE
     assert dsv4(L, q=MIS) == kvq.KVQ_ERR_ALIGN
     assert dsv4(L, kv=MIS) == kvq.KVQ_ERR_ALIGN
@@ -167,6 +178,33 @@ def test_binding_rejects_cpu_tensors(L):
     with pytest.raises(ValueError):
         kvq.fused_qk_norm_rope(x, 2, 1, 1, 128, 1e-6, w, w, torch.zeros(4, 128), True,
                                torch.zeros(2, dtype=torch.int64))
+
+
+def test_binding_rejects_short_operands(L):
+    """Sizes the C ABI cannot see (weights, tables, per-token arrays) are
+    checked by the binding before anything reaches the library."""
+    import torch
+    bf, i64 = torch.bfloat16, torch.int64
+    x = torch.zeros(2, 4 * 128, dtype=bf)
+    w = torch.zeros(128, dtype=bf)
+    cs = torch.zeros(4, 128)
+    pos = torch.zeros(2, dtype=i64)
+    with pytest.raises(ValueError, match="head_dim values"):
+        kvq.fused_qk_norm_rope(x, 2, 1, 1, 128, 1e-6, w[:64], w, cs, True, pos)
+    with pytest.raises(ValueError, match="one value per token"):
+        kvq.fused_qk_norm_rope(x, 2, 1, 1, 128, 1e-6, w, w, cs, True, pos[:1])
+    q = torch.zeros(2, 3, 512, dtype=bf)
+    kv = torch.zeros(2, 512, dtype=bf)
+    w5 = torch.zeros(512, dtype=bf)
+    cs5 = torch.zeros(8, 64)
+    cache = torch.zeros(1, 64, 584, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="512 values"):
+        kvq.dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, 1e-6, w5[:256], w5, cs5, pos, pos, cache)
+    with pytest.raises(ValueError, match=r"\[max_pos, 64\]"):
+        kvq.dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, 1e-6, w5, w5, cs5[:, :32], pos, pos,
+                                                 cache)
+    with pytest.raises(ValueError, match="one value per token"):
+        kvq.dsv4_qnorm_rope_kv_rope_quant_insert(q, kv, 1e-6, w5, w5, cs5, pos, pos[:1], cache)
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
