@@ -36,8 +36,8 @@ constexpr int64_t kQkSmallRows = 152 * 8;
 // the TMA-staged shape; below, the register-pipelined (head_dim 128, full
 // NeoX) or one-shot general kernel.  Measured on GB300 with each launch
 // following a 512 MB write (as the QKV projection precedes this operator):
-// from 160 MB of rows the staged kernel is 6-13 % faster at every layout but
-// one (head_dim 128 with 64 rotated dims: 3 % slower), and ties at 80 MB;
+// from 160 MB of rows the staged kernel is 5-13 % faster at every layout,
+// and ties at 80 MB;
 // it also holds its time after any preceding kernel (111-113 us at 32768
 // tokens x 40 heads), while the one-shot kernels run 106-127 us depending
 // on the L2 contents they start from.
