@@ -14,6 +14,9 @@ GB/s.  Inputs are resident in HBM and larger than L2 (129 MB), so no L2 flush
 is needed between steps.
 
 The line also carries:
+  * config.core_gbs: the step's rate counted without the cos/sin rows,
+    positions, slots and weights (a narrower byte count beside the full one);
+  * cpu_baseline.one_thread: the oracle on one host thread, on a token sample;
   * per_config: every workload the benchmark configurations name (the
     17-token and 32768-token packed-QKV cases, the 16-token and 32768-token
     DSV4 cases and each point of the DSV4 token sweep), each under the
@@ -72,6 +75,17 @@ def dsv4_bytes(T, H, mapped):
     position and slot (int64) per token; 584 bytes per mapped token written;
     the two weight vectors once."""
     return T * (H * 512 * 2 * 2 + 512 * 2 + 64 * 4 + 8 + 8) + mapped * 584 + 2 * 512 * 2
+
+
+def core_bytes(qk, ds):
+    """The step's bytes without the per-token cos/sin rows, positions, slots
+    and the weights: Q/K rows read + written, q rows read + written, kv
+    vectors read, entries written (the pages define no byte count of their
+    own, so this narrower one is reported beside the full one)."""
+    T, Hq, Hk, D = qk["qkv"].shape[0], qk["Hq"], qk["Hk"], qk["D"]
+    Tq, H = ds["q"].shape[0], ds["H"]
+    mapped = int((ds["slot_mapping"] >= 0).sum())
+    return T * (Hq + Hk) * D * 4 + Tq * (H * 512 * 4 + 1024) + mapped * 584
 
 
 def step_bytes(qk, ds):
@@ -396,6 +410,25 @@ def cpu_baseline(qk, ds, qk_h, ds_h):
     return (b_qk + b_ds) / dt / 1e9, oracle.default_threads(), dt
 
 
+def cpu_baseline_one_thread(qk, ds, qk_h, ds_h, tokens=1024):
+    """The oracle on one host thread, on the first `tokens` tokens of each
+    operator.  Returns (GB/s by the same byte model, tokens, seconds)."""
+    import oracle
+    S = min(tokens, qk_h["qkv"].shape[0], ds_h["q"].shape[0])
+    cache = ds_h["kv_cache"].copy()
+    t0 = time.perf_counter()
+    oracle.qk_norm_rope(qk_h["qkv"][:S], qk["Hq"], qk["Hk"], qk["Hv"], qk["D"], qk["eps"],
+                        qk_h["q_weight"], qk_h["k_weight"], qk_h["cos_sin"],
+                        qk_h["positions"][:S], nthreads=1)
+    oracle.dsv4(ds_h["q"][:S], ds_h["kv"][:S], ds["eps"], ds_h["q_weight"], ds_h["kv_weight"],
+                ds_h["cos_sin"], ds_h["positions"][:S], ds_h["slot_mapping"][:S], cache,
+                nthreads=1)
+    dt = time.perf_counter() - t0
+    nb = (qk_bytes(S, qk["Hq"], qk["Hk"], qk["D"])
+          + dsv4_bytes(S, ds["H"], int((ds_h["slot_mapping"][:S] >= 0).sum())))
+    return nb / dt / 1e9, S, dt
+
+
 # ---------------------------------------------------------------------------
 # context: the unfused PyTorch baseline (separate eager passes on the GPU)
 # ---------------------------------------------------------------------------
@@ -712,10 +745,14 @@ def run_gpu(args):
     cpu = None
     if host_inputs is not None:
         v, cores, dt = cpu_baseline(qk, ds, *host_inputs)
+        v1, s1, dt1 = cpu_baseline_one_thread(qk, ds, *host_inputs)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "one whole step (both operators, all 32768 tokens, the same input "
                          "bytes as the GPU step), fp64 oracle, all host cores",
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2),
+               "one_thread": {"value": round(v1, 4), "unit": UNIT, "tokens": s1,
+                              "seconds": round(dt1, 2),
+                              "sample": f"the first {s1} tokens of each operator, one thread"}}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(ms_step, 5),
@@ -727,6 +764,10 @@ def run_gpu(args):
                             "launch (those events cost the launch overlap, so the step time "
                             "comes from the first pass, which has none)",
             "qk_gbs": round(b_qk / (qk_avg * 1e-3) / 1e9, 1),
+            "core_bytes_per_step": core_bytes(qk, ds),
+            "core_gbs": round(world * core_bytes(qk, ds) / (ms_step * 1e-3) / 1e9, 2),
+            "core_bytes": "Q/K rows, q rows and kv vectors read, rows and cache entries "
+                          "written; without cos/sin rows, positions, slots and weights",
             "qk_kernel": kvq.configs("qk")[kvq.qk_config_for(32768, 32, 8)],
             "pct_of_peak": round(100 * value / world / peak, 2),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),

@@ -101,3 +101,25 @@ def test_oracle_gbs_on_a_sample():
     d = wl.make_qk(20, 4, 2, 2, max_pos=64, seed=6)
     g, S = bench.oracle_gbs("qk", d, 64)
     assert S == 20 and g > 0
+
+
+def test_core_bytes_leave_out_tables_indices_and_weights():
+    """The narrower byte count differs from the full one by exactly the
+    per-token cos/sin rows, positions and slots, and the weight vectors."""
+    import workloads as wl
+    qk = wl.make_qk(12, 4, 2, 2, max_pos=64, seed=7)
+    ds = wl.make_dsv4(10, 3, max_pos=4096, num_blocks=4, block_size=32, slots="distinct_skip2",
+                      seed=8)
+    b_qk, b_ds = bench.step_bytes(qk, ds)
+    tables = 12 * (128 * 4 + 8) + 2 * 128 * 2 + 10 * (64 * 4 + 16) + 2 * 512 * 2
+    assert bench.core_bytes(qk, ds) == b_qk + b_ds - tables
+    assert bench.core_bytes(qk, ds) == 12 * 6 * 128 * 4 + 10 * (3 * 2048 + 1024) + 8 * 584
+
+
+def test_one_thread_oracle_baseline():
+    import workloads as wl
+    qk = wl.make_qk(12, 4, 2, 2, max_pos=64, seed=7)
+    ds = wl.make_dsv4(10, 3, max_pos=4096, num_blocks=4, block_size=32, slots="distinct_skip2",
+                      seed=8)
+    g, S, dt = bench.cpu_baseline_one_thread(qk, ds, *bench.host_step_inputs(qk, ds), tokens=8)
+    assert S == 8 and g > 0 and dt > 0
