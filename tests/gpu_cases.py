@@ -54,6 +54,39 @@ def qk_parity(d, slice_tokens=4096, call=None) -> Bf16Report:
     return rep
 
 
+def qk_parity_sampled(d, sample, seed=0, call=None) -> Bf16Report:
+    """Like qk_parity for workloads too large to compare whole: the first and
+    last 8 tokens and `sample` random ones against the oracle; V checked
+    bit-identical for every token on the GPU."""
+    Hq, Hk, Hv, D = d["Hq"], d["Hk"], d["Hv"], d["D"]
+    rot, neox = d.get("rot", D), d.get("is_neox", True)
+    T = d["qkv"].shape[0]
+    NR = Hq + Hk
+    qkv_in = d["qkv"].clone()
+    if call is None:
+        kvq.fused_qk_norm_rope(d["qkv"], Hq, Hk, Hv, D, d["eps"], d["q_weight"], d["k_weight"],
+                               d["cos_sin"], neox, d["positions"], rotary_dim=rot)
+    else:
+        call(d)
+    torch.cuda.synchronize()
+    v_cols = slice(NR * D, (NR + Hv) * D)
+    assert torch.equal(d["qkv"][:, v_cols], qkv_in[:, v_cols]), "V changed"
+    rng = np.random.default_rng(seed)
+    idx = np.unique(np.concatenate([np.arange(min(8, T)), np.arange(max(T - 8, 0), T),
+                                    rng.choice(T, size=min(sample, T), replace=False)]))
+    idx_t = torch.from_numpy(idx).to(d["qkv"].device)
+    inp = wl.bf16_bits(qkv_in.index_select(0, idx_t))
+    gpu = wl.bf16_bits(d["qkv"].index_select(0, idx_t)).reshape(idx.size, NR + Hv, D)
+    out, ref, mag = oracle.qk_norm_rope(inp, Hq, Hk, Hv, D, d["eps"], wl.bf16_bits(d["q_weight"]),
+                                        wl.bf16_bits(d["k_weight"]), wl.host(d["cos_sin"]),
+                                        np.ascontiguousarray(wl.host(d["positions"])[idx]),
+                                        is_neox=neox, rot_dim=rot, want_ref=True)
+    rep = Bf16Report()
+    rep.add(gpu[:, :NR], out.reshape(idx.size, NR + Hv, D)[:, :NR], ref, mag)
+    rep.check("fused_qk_norm_rope")
+    return rep
+
+
 # ---------------------------------------------------------------------------
 # DSV4 operator
 # ---------------------------------------------------------------------------

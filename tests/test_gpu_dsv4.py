@@ -245,6 +245,41 @@ def test_gather_hand_entry(cuda_device):
                        torch.tensor(np.repeat(block_w + [1.0], 64), dtype=torch.float32))
 
 
+def test_cache_beyond_4_gib(cuda_device, parity_log):
+    """A 4.9 GB cache (131072 blocks of 64 slots): every token maps to one of
+    the last 4096 slots (entry offsets past 2^32 bytes, the very last slot
+    included), through both launch shapes; then the entries are read back by
+    the gather, bit-exact against the oracle's reading of the same bytes."""
+    import oracle
+    n = 131072 * 64
+    assert (n - 4096) * 584 > 2**32
+    for threshold in (SMALL_PATH, TILED_PATH):
+        d = wl.make_dsv4(4096, 8, max_pos=131072, num_blocks=131072, block_size=64, seed=78,
+                         device=cuda_device)
+        g = torch.Generator(device=cuda_device).manual_seed(79)
+        slots = n - 1 - torch.randperm(4096, generator=g, device=cuda_device)
+        slots[[5, 2000]] = -1
+        d["slot_mapping"] = slots
+        with with_threshold(threshold):
+            qrep, crep = dsv4_parity(d, sample=1024, seed=80)
+        assert crep.exp_mismatch_ties == 0
+        parity_log(qrep, crep)
+        # read back: the entries at the sampled slots, compared through a
+        # small host copy of exactly those entries
+        read = torch.cat([slots[:64], torch.tensor([n - 1, -1], device=cuda_device)])
+        out = kvq.dsv4_kv_cache_gather(d["kv_cache"], read)
+        torch.cuda.synchronize()
+        flat = d["kv_cache"].view(-1, 584)
+        mapped = read >= 0
+        small = torch.zeros((int(read.numel()), 584), dtype=torch.uint8, device=cuda_device)
+        small[mapped] = flat[read[mapped]]
+        local = torch.where(mapped, torch.arange(read.numel(), device=cuda_device), -1)
+        want = oracle.dsv4_gather(wl.host(small).reshape(1, -1, 584), wl.host(local))
+        assert np.array_equal(wl.bf16_bits(out), want)
+        del d, slots, out, flat, small
+        torch.cuda.empty_cache()
+
+
 # ---- separate q output and CUDA-graph capture -------------------------------
 
 @pytest.mark.parametrize("T,H,threshold", [(16, 64, None), (777, 5, TILED_PATH),

@@ -5,7 +5,7 @@ import torch
 
 import kv_quant_cache_gb300 as kvq
 import workloads as wl
-from gpu_cases import qk_parity, to_device, with_config
+from gpu_cases import qk_parity, qk_parity_sampled, to_device, with_config
 
 pytestmark = pytest.mark.gpu
 
@@ -262,6 +262,36 @@ def test_staged_shape_at_131072_tokens(cuda_device):
     rep = qk_parity(d, slice_tokens=16384)
     assert rep.n == 131072 * 40 * 128
     assert kvq.stage_events(reset=True) == (0, 0)
+
+
+@pytest.mark.parametrize("config", [-1, 2, 4, 5, 10],
+                         ids=["auto", "tiles4", "stream", "general", "tile"])
+def test_offsets_beyond_4_gib(cuda_device, config, parity_log):
+    """360000 tokens x 48 heads x 128 dims: qkv is 4.42 GB, so element offsets
+    pass 2^31 and byte offsets 2^32.  Every launch family; the first and last
+    tokens and 1024 random ones against the oracle, V unchanged everywhere."""
+    T = 360000
+    assert T * 48 * 128 > 2**31 and T * 48 * 128 * 2 > 2**32
+    d = wl.make_qk(T, 32, 8, 8, theta=1e6, max_pos=131072, seed=4242, device=cuda_device)
+    with with_config("qk", config):
+        rep = qk_parity_sampled(d, 1024, seed=config + 1)
+    parity_log(rep)
+    del d
+    torch.cuda.empty_cache()
+
+
+def test_general_layout_offsets_beyond_4_gib(cuda_device, parity_log):
+    """head_dim 256, GPT-J pairs, 64 rotated dims, 180000 tokens (4.42 GB of
+    qkv), through the automatic (staged) shape and the one-shot kernel."""
+    T = 180000
+    for config in (-1, 5):
+        d = wl.make_qk(T, 32, 8, 8, D=256, theta=1e6, max_pos=131072, seed=4343,
+                       device=cuda_device, rotary_dim=64, is_neox=False)
+        with with_config("qk", config):
+            rep = qk_parity_sampled(d, 1024, seed=config + 7)
+        parity_log(rep)
+        del d
+        torch.cuda.empty_cache()
 
 
 @pytest.mark.skipif(not torch.cuda.is_available() or torch.cuda.device_count() < 2,
