@@ -1143,7 +1143,8 @@ def sweep(kvq, device):
 def run_profile_case(args):
     """A reduced case of one kernel for profiler captures: --profile qk|dsv4,
     --tokens T, --heads H, --launches n (each launch on the same inputs),
-    --shape NAME (a launch shape by its name; default: the automatic one)."""
+    --shape NAME (a launch shape by its name; default: the automatic one);
+    for qk also --head-dim, --rotary-dim (default: the head dim) and --gptj."""
     import kv_quant_cache_gb300 as kvq
     device = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(device)
@@ -1153,14 +1154,21 @@ def run_profile_case(args):
             raise SystemExit(f"--shape: {args.shape!r} is not one of {names}")
         kvq.set_config(args.profile, names.index(args.shape))
     if args.profile == "qk":
-        d = wl.make_qk(args.tokens, args.heads, 8, 8, theta=1e6, max_pos=131072, seed=1001,
-                       device=device)
-        fn, nb = (lambda: launch_qk(kvq, d, stream)), qk_bytes(args.tokens, args.heads, 8)
+        D = args.head_dim
+        rot = D if args.rotary_dim is None else args.rotary_dim
+        d = wl.make_qk(args.tokens, args.heads, 8, 8, D=D, theta=1e6, max_pos=131072, seed=1001,
+                       device=device, rotary_dim=rot, is_neox=not args.gptj)
+        fn = lambda: kvq.fused_qk_norm_rope(  # noqa: E731
+            d["qkv"], args.heads, 8, 8, D, d["eps"], d["q_weight"], d["k_weight"], d["cos_sin"],
+            not args.gptj, d["positions"], stream=stream, rotary_dim=rot)
+        nb = qk_bytes(args.tokens, args.heads, 8, D, rot)
     else:
         d = wl.make_dsv4(args.tokens, args.heads, max_pos=131072,
                          num_blocks=-(-2 * args.tokens // 64), block_size=64, seed=1003,
                          device=device)
         fn, nb = (lambda: launch_dsv4(kvq, d, stream)), dsv4_bytes(args.tokens, args.heads, args.tokens)
+    fn()  # the first call does the per-device set-up; time the later ones
+    torch.cuda.synchronize(device)
     med, best = _time_launch(fn, args.launches, stream)
     print(json.dumps({"profile": args.profile, "tokens": args.tokens, "heads": args.heads,
                       "bytes": nb, "us_median": round(med * 1e3, 2),
@@ -1190,6 +1198,9 @@ def main():
     ap.add_argument("--heads", type=int, default=64)
     ap.add_argument("--launches", type=int, default=5)
     ap.add_argument("--shape", default=None)
+    ap.add_argument("--head-dim", type=int, default=128)
+    ap.add_argument("--rotary-dim", type=int, default=None)
+    ap.add_argument("--gptj", action="store_true")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args)
