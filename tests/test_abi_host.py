@@ -171,6 +171,22 @@ def test_dispatch_threshold(L):
         kvq.set_dsv4_dispatch_threshold(old)
 
 
+@pytest.mark.parametrize("value,expected", [("1234", 1234), ("0", 0), ("abc", 65536),
+                                            ("-5", 65536), ("12x", 65536), ("", 65536)])
+def test_dispatch_threshold_from_environment(L, value, expected):
+    """KVQ_DSV4_DISPATCH_THRESHOLD is read once, in a fresh process; anything
+    but a plain non-negative integer leaves the built-in default."""
+    import subprocess
+    import sys
+    env = dict(os.environ, KVQ_DSV4_DISPATCH_THRESHOLD=value)
+    code = ("import ctypes, sys; L = ctypes.CDLL(sys.argv[1]); "
+            "L.kvq_dsv4_dispatch_threshold.restype = ctypes.c_int64; "
+            "print(L.kvq_dsv4_dispatch_threshold())")
+    out = subprocess.run([sys.executable, "-c", code, kvq.LIB_PATH], env=env, check=True,
+                         capture_output=True, text=True).stdout
+    assert int(out) == expected
+
+
 def test_binding_rejects_cpu_tensors(L):
     import torch
     x = torch.zeros(2, 4 * 128, dtype=torch.bfloat16)
