@@ -2,7 +2,7 @@
 
 The GPU tests trust these reports, so each rule is checked here: what counts
 as within one bf16 ulp, when the cancellation allowance applies and is
-counted, and how exponent bytes and e4m3 codes are judged.
+counted, and how exponent bytes and e4m3 codes are compared.
 """
 import math
 
