@@ -114,7 +114,8 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
  *   num_heads_q/k/v  >= 0 each.
  *   head_dim       64, 128 or 256 (else KVQ_ERR_UNSUPPORTED).
  *   eps            added to the mean square inside the square root; finite,
- *                  >= 0.
+ *                  >= 0.  With eps = 0 an all-zero head row has no norm
+ *                  (0/0): its outputs are NaN.
  *   q_weight, k_weight  bf16 [head_dim] RMSNorm weights, 16-byte aligned.
  *   cos_sin_cache  fp32 [max_pos, rotary_dim]; row p holds cos(p * f_i) for
  *                  i < rotary_dim/2 followed by sin(p * f_i); 16-byte aligned.
@@ -160,7 +161,9 @@ kvq_status fused_qk_norm_rope_ex(void* qkv, int64_t num_tokens, int num_heads_q,
  *   kv             bf16 [num_tokens, 512], contiguous, 16-byte aligned; read
  *                  only.
  *   num_tokens     T >= 0; num_heads H >= 1 (T * (H + 1) below 2^31).
- *   eps            finite, >= 0.
+ *   eps            finite, >= 0.  With eps = 0 an all-zero q row comes out
+ *                  NaN, and the cache entry of an all-zero kv vector is
+ *                  unspecified (0/0 has no norm).
  *   q_weight, kv_weight  bf16 [512], 16-byte aligned.
  *   cos_sin_cache  fp32 [max_pos, 64]: 32 cosines then 32 sines per row;
  *                  16-byte aligned.

@@ -69,6 +69,43 @@ def test_zero_rows_and_tiny_values(cuda_device):
     qk_parity(to_device(d, cuda_device))
 
 
+@pytest.mark.parametrize("config", [-1, 2, 5, 7], ids=["auto", "tiles4", "general", "bulk"])
+def test_eps_zero_all_zero_rows_are_nan(cuda_device, config):
+    """eps = 0: an all-zero head row has no norm (0/0).  The oracle gives NaN
+    there and so must every launch family; the other rows match the oracle
+    and V is untouched."""
+    import oracle
+    from parity import Bf16Report
+    T, Hq, Hk, Hv, D = 24, 4, 2, 2, 128
+    d = wl.make_qk(T, Hq, Hk, Hv, max_pos=64, seed=21, device="cpu", eps=0.0)
+    x = d["qkv"].float()
+    x[[3, 17]] = 0.0
+    d["qkv"] = x.to(torch.bfloat16)
+    inp = wl.bf16_bits(d["qkv"])
+    g = to_device(d, cuda_device)
+    with with_config("qk", config):
+        kvq.fused_qk_norm_rope(g["qkv"], Hq, Hk, Hv, D, 0.0, g["q_weight"], g["k_weight"],
+                               g["cos_sin"], True, g["positions"])
+    torch.cuda.synchronize()
+    gpu = wl.bf16_bits(g["qkv"]).reshape(T, Hq + Hk + Hv, D)
+    out, ref, mag = oracle.qk_norm_rope(inp, Hq, Hk, Hv, D, 0.0, wl.bf16_bits(d["q_weight"]),
+                                        wl.bf16_bits(d["k_weight"]), wl.host(d["cos_sin"]),
+                                        wl.host(d["positions"]), want_ref=True)
+    out = out.reshape(T, Hq + Hk + Hv, D)
+    NR = Hq + Hk
+
+    def isnan(b):
+        return ((b & 0x7f80) == 0x7f80) & ((b & 0x7f) != 0)
+    zero = np.zeros(T, bool)
+    zero[[3, 17]] = True
+    assert isnan(out[zero, :NR]).all() and isnan(gpu[zero, :NR]).all()
+    assert not isnan(gpu[~zero, :NR]).any()
+    assert np.array_equal(gpu[:, NR:], inp.reshape(T, -1, D)[:, NR:])
+    rep = Bf16Report()
+    rep.add(gpu[~zero, :NR], out[~zero, :NR], ref[~zero], mag[~zero])
+    rep.check("fused_qk_norm_rope, eps = 0")
+
+
 def test_zero_tokens_is_a_no_op(cuda_device):
     d = wl.make_qk(0, 2, 1, 1, device=cuda_device)
     kvq.fused_qk_norm_rope(d["qkv"], 2, 1, 1, 128, 1e-6, d["q_weight"], d["k_weight"],
