@@ -73,6 +73,45 @@ def test_all_tokens_unmapped(cuda_device):
     assert crep.entries == 0
 
 
+@pytest.mark.parametrize("threshold", [SMALL_PATH, TILED_PATH], ids=["small", "tiled"])
+def test_eps_zero_all_zero_q_rows_are_nan(cuda_device, threshold):
+    """eps = 0: all-zero q rows (tokens 2 and 9, which have no cache slot)
+    come out NaN, as in the oracle; every other q row and every written
+    cache entry matches the oracle, and no other cache byte changes."""
+    import oracle
+    from parity import Bf16Report, compare_cache
+    T, H = 12, 3
+    d = wl.make_dsv4(T, H, max_pos=4096, num_blocks=1, block_size=32, seed=31, device="cpu",
+                     eps=0.0)
+    q = d["q"].float()
+    q[[2, 9]] = 0.0
+    d["q"] = q.to(torch.bfloat16)
+    d["slot_mapping"][[2, 9]] = -1
+    q_in, cache_in = wl.bf16_bits(d["q"]), wl.host(d["kv_cache"]).copy()
+    g = to_device(d, cuda_device)
+    with with_threshold(threshold):
+        run_dsv4(g)
+    torch.cuda.synchronize()
+    res = oracle.dsv4(q_in, wl.bf16_bits(d["kv"]), 0.0, wl.bf16_bits(d["q_weight"]),
+                      wl.bf16_bits(d["kv_weight"]), wl.host(d["cos_sin"]),
+                      wl.host(d["positions"]), wl.host(d["slot_mapping"]), cache_in,
+                      want_ref=True)
+    gq = wl.bf16_bits(g["q"])
+
+    def isnan(b):
+        return ((b & 0x7f80) == 0x7f80) & ((b & 0x7f) != 0)
+    zero = np.zeros(T, bool)
+    zero[[2, 9]] = True
+    assert isnan(res["q"][zero]).all() and isnan(gq[zero]).all()
+    assert not isnan(gq[~zero]).any()
+    rep = Bf16Report()
+    rep.add(gq[~zero], res["q"][~zero], res["q_ref"][~zero], res["q_mag"][~zero])
+    rep.check("dsv4 q, eps = 0")
+    crep = compare_cache(wl.host(g["kv_cache"]), cache_in, wl.host(d["slot_mapping"]),
+                         res["kv_ref"], res["kv_mag"], res["exp_margin"])
+    crep.check("dsv4 cache, eps = 0")
+
+
 def test_last_slot_and_last_position(cuda_device):
     d = wl.make_dsv4(4, 2, max_pos=4096, num_blocks=3, block_size=8, seed=8, device=cuda_device)
     d["slot_mapping"] = torch.tensor([23, 0, -1, 22], dtype=torch.int64, device=cuda_device)
