@@ -134,8 +134,9 @@ kvq_status fused_qk_norm_rope(void* qkv, int64_t num_tokens, int num_heads_q,
  * so the partner enters with its own dimension's weight.  head_dim 128 with
  * full NeoX rotation runs tuned register-pipelined kernels, the other
  * layouts a general one; batches of 128 MiB of Q+K rows and more, in every
- * layout, take a kernel that stages rows through shared memory with the
- * bulk-copy (TMA) engine (launch shapes below).  The staged kernel computes
+ * layout (and from 56 MiB at head_dim 128 with full NeoX rotation), take a
+ * kernel that stages rows through shared memory with the bulk-copy (TMA)
+ * engine (launch shapes below).  The staged kernel computes
  * 1/sqrt correctly rounded, the others with the hardware approximation
  * (within 2 fp32 ulp), each the form it runs fastest with; outputs of the two
  * are equal but for rare values (about 1 in 10^5), each within the stated
@@ -296,9 +297,11 @@ int kvq_dsv4_dispatch_path(int64_t num_tokens, int num_heads);
  * (approximate vs correctly rounded; see fused_qk_norm_rope_ex).
  * Configuration 6 (general, 8-dim fragments) also adds the sum of squares in
  * another order.  Automatic choice: below 1216 Q+K rows the small-batch
- * shape, below 128 MiB of Q+K rows (rows x head_dim x 2) the
- * register-pipelined shape (head_dim 128, full NeoX) or the general kernel,
- * from there on the staged shape (kvq_qk_config_for describes head_dim 128).
+ * shape; below 128 MiB of Q+K rows (rows x head_dim x 2) the
+ * register-pipelined shape (head_dim 128, full NeoX; from 56 MiB on the
+ * 24-warp staged shape bulk<24w,2st,3KB> instead) or the general kernel
+ * (other layouts); from there on the staged shape bulk<16w,2st,6KB>
+ * (kvq_qk_config_for describes head_dim 128, full NeoX).
  *   *_num_configs   number of configurations
  *   *_config_name   static name of configuration id (NULL if out of range)
  *   kvq_set_*_config  force id (0 <= id < num) or restore automatic (id < 0);

@@ -24,6 +24,7 @@ constexpr int kDsv4LargeConfig = 4;  // stream<8w,85reg,pairs>
 constexpr int kQkSmallConfig = 0;    // tiles<4w,1step>
 constexpr int kQkLargeConfig = 2;    // tiles<4w,4step>
 constexpr int kQkStagedConfig = 7;   // bulk<16w,2st,6KB>
+constexpr int kQkMidStagedConfig = 8;  // bulk<24w,2st,3KB>
 // Entries of kQkConfigs that name the general kernel (any layout) with 4- or
 // 8-dim fragments; forcing one routes every layout through that kernel.
 constexpr int kQkGeneralFrag4Config = 5;
@@ -42,6 +43,13 @@ constexpr int64_t kQkSmallRows = 152 * 8;
 // tokens x 40 heads), while the one-shot kernels run 106-127 us depending
 // on the L2 contents they start from.
 constexpr int64_t kQkStagedBytes = (int64_t)1 << 27;
+// Head_dim 128 with full NeoX rotation only: from 56 MiB of Q+K rows the
+// 24-warp staged shape with 3 KB stages is 3-6 % faster than the
+// register-pipelined kernel after a 512 MB write (GB300, two boxes, 32/8/8
+// heads: T = 6144 29.4 vs 30.3-30.7 us, T = 8192 35.1 vs 37.1 us, T = 12288
+// 49.4 vs 52.3-52.5 us; at T = 5120 the two tie within 2 % either way); the
+// one-shot general kernel of the other layouts keeps its lead there.
+constexpr int64_t kQkMidStagedBytes = (int64_t)56 << 20;
 
 std::atomic<int64_t> g_threshold{-1};
 std::atomic<int> g_dsv4_config{-1};
@@ -78,14 +86,15 @@ kvq_status finish_launch(cudaError_t e) {
 
 constexpr int64_t kIndexLimit = (int64_t)1 << 31;
 
-int qk_config_for(int64_t num_tokens, int64_t rows, int head_dim) {
+int qk_config_for(int64_t num_tokens, int64_t rows, int head_dim, bool tuned) {
   const int forced = g_qk_config.load(std::memory_order_relaxed);
   if (forced >= 0) return forced;
   if (num_tokens >= kIndexLimit || rows >= kIndexLimit) return kQkStagedConfig;
   const int64_t n = num_tokens * rows;
-  return n < kQkSmallRows                        ? kQkSmallConfig
-         : n * head_dim * 2 < kQkStagedBytes ? kQkLargeConfig
-                                                 : kQkStagedConfig;
+  const int64_t bytes = n * head_dim * 2;
+  if (n < kQkSmallRows) return kQkSmallConfig;
+  if (bytes >= kQkStagedBytes) return kQkStagedConfig;
+  return tuned && bytes >= kQkMidStagedBytes ? kQkMidStagedConfig : kQkLargeConfig;
 }
 
 int dsv4_config_for(int64_t num_tokens, int num_heads) {
@@ -180,7 +189,7 @@ kvq_status qk_impl(void* qkv, int64_t num_tokens, int num_heads_q, int num_heads
   const int64_t n = num_tokens * (int64_t)rows;
   const bool small = n < kQkSmallRows;
   const bool tuned = head_dim == 128 && is_neox == 1 && rotary_dim == 128;
-  const int config = qk_config_for(num_tokens, rows, head_dim);
+  const int config = qk_config_for(num_tokens, rows, head_dim, tuned);
   if (config == kQkGeneralFrag4Config || config == kQkGeneralFrag8Config)
     return finish_launch(
         kvq::launch_qk_general(a, small, config == kQkGeneralFrag8Config ? 8 : 4, st));
@@ -401,7 +410,7 @@ const char* kvq_qk_config_name(int id) {
 int kvq_set_qk_config(int id) { return set_config(g_qk_config, id, kvq::kQkNumConfigs); }
 
 int kvq_qk_config_for(int64_t num_tokens, int num_heads_q, int num_heads_k) {
-  return qk_config_for(num_tokens, (int64_t)num_heads_q + num_heads_k, 128);
+  return qk_config_for(num_tokens, (int64_t)num_heads_q + num_heads_k, 128, true);
 }
 
 int kvq_dsv4_num_configs(void) { return kvq::kDsv4NumConfigs; }

@@ -262,7 +262,9 @@ def test_launch_config_table(L):
     assert qk[kvq.qk_config_for(17, 16, 8)] == "tiles<4w,1step>"
     assert qk[kvq.qk_config_for(30, 32, 8)] == "tiles<4w,1step>"   # 1200 rows
     assert qk[kvq.qk_config_for(31, 32, 8)] == "tiles<4w,4step>"   # 1240 rows
-    assert qk[kvq.qk_config_for(13107, 32, 8)] == "tiles<4w,4step>"   # 524280 rows
+    assert qk[kvq.qk_config_for(5734, 32, 8)] == "tiles<4w,4step>"    # 229360 rows < 56 MiB
+    assert qk[kvq.qk_config_for(5735, 32, 8)] == "bulk<24w,2st,3KB>"  # 229400 rows
+    assert qk[kvq.qk_config_for(13107, 32, 8)] == "bulk<24w,2st,3KB>"  # 524280 rows < 128 MiB
     assert qk[kvq.qk_config_for(13108, 32, 8)] == "bulk<16w,2st,6KB>"
     assert qk[kvq.qk_config_for(32768, 32, 8)] == "bulk<16w,2st,6KB>"
 
